@@ -1,0 +1,186 @@
+"""NumPy front end of the CPU oracle (``fp8_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU
+baseline leg use this module; the CUDA library never does. It builds ``liboracle.so`` from
+``fp8_oracle.c`` with gcc (no fast-math, no FP contraction) on first use.
+
+What each function computes, and the pages it follows, is documented in ``fp8_oracle.c``:
+fine-grained E4M3 quantization with one FP32 scale per 1x128 activation tile and per
+128x128 weight block (codingmall.com, "Định lượng hạt mịn" / "Định lượng trực tuyến"), and
+the block-scaled GEMM whose per-128-K-block partials are rescaled and accumulated in high
+precision (codingmall.com, "Tăng độ chính xác tích lũy"; dtcms.com, section 三.3).
+
+Arrays: BF16 tensors are passed as their uint16 bit patterns; codes are uint8 E4M3FN bytes;
+activation scales are float32 [K/128][M]; weight scales float32 [ceil(N/128)][K/128].
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "fp8_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_i64 = ctypes.c_int64
+_p = ctypes.c_void_p
+
+
+def build(force: bool = False) -> str:
+    """Compile fp8_oracle.c into liboracle.so (strict IEEE: no fast-math, no contraction)."""
+    if force or not os.path.exists(_LIB_PATH) or (
+            os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-std=c11", "-O2", "-Wall", "-Wextra", "-fno-fast-math", "-ffp-contract=off",
+             "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is None:
+            L = ctypes.CDLL(build())
+            L.orc_e4m3_decode.restype = ctypes.c_double
+            L.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
+            L.orc_e4m3_encode.restype = ctypes.c_uint8
+            L.orc_e4m3_encode.argtypes = [ctypes.c_float]
+            L.orc_e4m3_encode_array.argtypes = [_p, _i64, _p]
+            L.orc_e4m3_decode_array.argtypes = [_p, _i64, _p]
+            L.orc_quant_act_1x128.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p]
+            L.orc_quant_weight_128x128.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p]
+            L.orc_gemm_points.argtypes = [_p, _i64, _p, _p, _i64, _p, _i64, _i64, _i64,
+                                          _i64, _p, _p, _p, _p, _p]
+            L.orc_gemm_f64.argtypes = [_p, _i64, _p, _p, _i64, _p, _i64, _i64, _i64, _p, _p]
+            L.orc_grouped_gemm_points.argtypes = [_p, _i64, _p, _p, _i64, _p, _p, _i64, _i64,
+                                                  _i64, _i64, _i64, _p, _p, _p, _p]
+            L.orc_gemm_unquantized_f64.argtypes = [_p, _i64, _p, _i64, _i64, _i64, _i64, _p]
+            for f in (L.orc_e4m3_encode_array, L.orc_e4m3_decode_array, L.orc_quant_act_1x128,
+                      L.orc_quant_weight_128x128, L.orc_gemm_points, L.orc_gemm_f64,
+                      L.orc_grouped_gemm_points, L.orc_gemm_unquantized_f64):
+                f.restype = None
+            _lib = L
+        return _lib
+
+
+def _ptr(a: np.ndarray | None):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# --------------------------------------------------------------------------------------
+# E4M3
+# --------------------------------------------------------------------------------------
+
+def e4m3_decode(codes) -> np.ndarray:
+    c = _c(codes, np.uint8)
+    out = np.empty(c.shape, np.float64)
+    lib().orc_e4m3_decode_array(_ptr(c), c.size, _ptr(out))
+    return out
+
+
+def e4m3_encode(x) -> np.ndarray:
+    v = _c(x, np.float32)
+    out = np.empty(v.shape, np.uint8)
+    lib().orc_e4m3_encode_array(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+# --------------------------------------------------------------------------------------
+# Quantizers
+# --------------------------------------------------------------------------------------
+
+def quant_act_1x128(x_bits) -> tuple[np.ndarray, np.ndarray]:
+    """x_bits: uint16 BF16 bits [M][K]. Returns (codes uint8 [M][K], scales f32 [K/128][M])."""
+    x = _c(x_bits, np.uint16)
+    M, K = x.shape
+    assert K % 128 == 0
+    q = np.empty((M, K), np.uint8)
+    s = np.empty((K // 128, M), np.float32)
+    lib().orc_quant_act_1x128(_ptr(x), M, K, K, _ptr(q), K, _ptr(s))
+    return q, s
+
+
+def quant_weight_128x128(w_bits) -> tuple[np.ndarray, np.ndarray]:
+    """w_bits: uint16 BF16 bits [N][K]. Returns (codes [N][K], scales f32 [ceil(N/128)][K/128])."""
+    w = _c(w_bits, np.uint16)
+    N, K = w.shape
+    assert K % 128 == 0
+    q = np.empty((N, K), np.uint8)
+    s = np.empty(((N + 127) // 128, K // 128), np.float32)
+    lib().orc_quant_weight_128x128(_ptr(w), N, K, K, _ptr(q), K, _ptr(s))
+    return q, s
+
+
+# --------------------------------------------------------------------------------------
+# GEMMs
+# --------------------------------------------------------------------------------------
+
+def gemm_f64(aq, a_s, wq, w_s) -> tuple[np.ndarray, np.ndarray]:
+    """Whole C = A W^T in FP64 on the quantized operands, and sum_k |a_hat w_hat| per element."""
+    aq, wq = _c(aq, np.uint8), _c(wq, np.uint8)
+    a_s, w_s = _c(a_s, np.float32), _c(w_s, np.float32)
+    M, K = aq.shape
+    N = wq.shape[0]
+    c = np.empty((M, N), np.float64)
+    cabs = np.empty((M, N), np.float64)
+    lib().orc_gemm_f64(_ptr(aq), K, _ptr(a_s), _ptr(wq), K, _ptr(w_s), M, N, K,
+                       _ptr(c), _ptr(cabs))
+    return c, cabs
+
+
+def gemm_points(aq, a_s, wq, w_s, pm, pn, want_f32: bool = False):
+    """Selected elements (pm[i], pn[i]): returns (c64, cabs) or (c64, cabs, c32)."""
+    aq, wq = _c(aq, np.uint8), _c(wq, np.uint8)
+    a_s, w_s = _c(a_s, np.float32), _c(w_s, np.float32)
+    pm, pn = _c(pm, np.int64), _c(pn, np.int64)
+    M, K = aq.shape
+    N = wq.shape[0]
+    n = pm.size
+    c = np.empty(n, np.float64)
+    cabs = np.empty(n, np.float64)
+    c32 = np.empty(n, np.float32) if want_f32 else None
+    lib().orc_gemm_points(_ptr(aq), K, _ptr(a_s), _ptr(wq), K, _ptr(w_s), M, N, K,
+                          n, _ptr(pm), _ptr(pn), _ptr(c), _ptr(cabs), _ptr(c32))
+    return (c, cabs, c32) if want_f32 else (c, cabs)
+
+
+def grouped_gemm_points(aq, a_s, wq, w_s, offsets, pr, pn):
+    """Grouped GEMM elements. aq [R][K]; a_s [K/128][R]; wq [G][N][K]; w_s [G][NB][KB];
+    offsets int32 [G+1]. Returns (c64, cabs) at (pr[i], pn[i])."""
+    aq, wq = _c(aq, np.uint8), _c(wq, np.uint8)
+    a_s, w_s = _c(a_s, np.float32), _c(w_s, np.float32)
+    off = _c(offsets, np.int32)
+    pr, pn = _c(pr, np.int64), _c(pn, np.int64)
+    R, K = aq.shape
+    G, N = off.size - 1, wq.shape[1]
+    assert wq.shape[0] == G and w_s.shape[0] == G, "one weight matrix per group"
+    n = pr.size
+    c = np.empty(n, np.float64)
+    cabs = np.empty(n, np.float64)
+    lib().orc_grouped_gemm_points(_ptr(aq), K, _ptr(a_s), _ptr(wq), K, _ptr(w_s), _ptr(off),
+                                  G, R, N, K, n, _ptr(pr), _ptr(pn), _ptr(c), _ptr(cabs))
+    return c, cabs
+
+
+def gemm_unquantized_f64(x_bits, w_bits) -> np.ndarray:
+    x, w = _c(x_bits, np.uint16), _c(w_bits, np.uint16)
+    M, K = x.shape
+    N = w.shape[0]
+    c = np.empty((M, N), np.float64)
+    lib().orc_gemm_unquantized_f64(_ptr(x), K, _ptr(w), K, M, N, K, _ptr(c))
+    return c
