@@ -1,0 +1,432 @@
+#!/usr/bin/env python3
+"""Benchmark of the fine-grained FP8 hot path on one B300.
+
+One step = the whole path over one batch of the dense-projection workload
+(A = 4096 x 7168 BF16 activations, W = 18432 x 7168 BF16 weights):
+  1. fp8_quant_act_1x128       A -> E4M3 codes + FP32 scales per 1x128 tile
+  2. fp8_quant_weight_128x128  W -> E4M3 codes + FP32 scales per 128x128 block
+  3. fp8_blockscaled_gemm      C = A W^T, per-128-K promotion into FP32, BF16 output
+The metric is block-scaled FP8 GEMM throughput in TFLOP/s (2*M*N*K per step divided by the
+step time, quantizers included); per-kernel GB/s and TFLOP/s against the rooflines ride along.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs an independent replica of the step (the path needs no
+exchange between GPUs); the reported time is the maximum over ranks and `value` counts the work
+of all ranks. `--impl reference` times the CPU oracle (plain C, the correctness reference) on a
+bounded sample of the same workload on the host cores (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from fp8_fine_grained_23_b300 import workloads as WL  # noqa: E402
+
+METRIC = "block-scaled FP8 GEMM TFLOPS (% FP8 peak); quantizer GB/s (% HBM), 1 B300"
+SHAPE = WL.DENSE
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+FP8_OVER_BF16 = 2.0      # nominal dense ratio on B300: 4.5 / 2.25 PFLOP/s
+ACT_BYTES_PER_ELEM = 2 + 1 + 4 / 128      # BF16 read, code write, one FP32 scale per 128
+W_BYTES_PER_ELEM = 2 + 1 + 4 / (128 * 128)
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def gemm_flops(M, N, K):
+    return 2.0 * M * N * K
+
+
+# --------------------------------------------------------------------------------------
+# Clock sampling during the timed region
+# --------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = None
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            self.ident = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            self.ident = str(device_index)
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.ident, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == 8:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+
+        sm = [num(r[0]) for r in rows]
+        mx = [num(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "power_w_max": max(num(r[2]) for r in rows), "samples": len(rows),
+                "reasons": reasons}
+
+
+# --------------------------------------------------------------------------------------
+# Our path
+# --------------------------------------------------------------------------------------
+
+def traffic_from_profile():
+    """DRAM bytes per GEMM launch from the committed ncu summary, if it was taken on the
+    current kernel source (matching SHA-256); otherwise None."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "gemm_dense_4096x18432x7168.txt")
+    src = os.path.join(ROOT, "fp8_fine_grained_23_b300", "csrc", "gemm.cu")
+    try:
+        kv = {}
+        for line in open(path):
+            if "=" in line and not line.startswith("#"):
+                k, v = line.split("=", 1)
+                kv[k.strip()] = v.strip()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        if kv.get("gemm_cu_sha256") != sha:
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def run_ours(args, rank, world, local_rank):
+    from fp8_fine_grained_23_b300 import build as B
+    if rank == 0 or not os.path.exists(B.LIB_PATH):
+        B.build()
+    if world > 1:
+        torch.distributed.barrier()
+    from fp8_fine_grained_23_b300 import fp8bs as F
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    M, N, K = SHAPE.M, SHAPE.N, SHAPE.K
+    a, w = WL.gemm_inputs(SHAPE, dev)
+    aq = torch.empty(M, K, dtype=torch.uint8, device=dev)
+    a_s = torch.empty(K // 128, M, dtype=torch.float32, device=dev)
+    wq = torch.empty(N, K, dtype=torch.uint8, device=dev)
+    w_s = torch.empty((N + 127) // 128, K // 128, dtype=torch.float32, device=dev)
+    c = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        F.fp8_quant_act_1x128(a, aq, a_s, stream=sh)
+        if ev is not None:
+            ev[1].record(stream)
+        F.fp8_quant_weight_128x128(w, wq, w_s, stream=sh)
+        if ev is not None:
+            ev[2].record(stream)
+        F.fp8_blockscaled_gemm(aq, a_s, wq, w_s, out=c, stream=sh)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if F.fp8bs_last_error(sh) != F.FP8BS_OK:
+        raise RuntimeError("a kernel reported a pipeline timeout during warm-up")
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local_rank)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)                        # let the sampler take its first readings
+    t0.record(stream)
+    for i in range(args.steps):
+        step(events[i])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    if F.fp8bs_last_error(sh) != F.FP8BS_OK:
+        raise RuntimeError("a kernel reported a pipeline timeout in the timed region")
+
+    ms = t0.elapsed_time(t1) / args.steps
+    k_ms = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in events) for j in range(3)]
+    t = torch.tensor([ms] + k_ms, dtype=torch.float64)
+    if world > 1:
+        tt = t.to(dev) if torch.distributed.get_backend() == "nccl" else t
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        t = tt.cpu()
+    ms, qa_ms, qw_ms, g_ms = t.tolist()
+
+    # end to end through the C ABI from pinned host buffers: H2D of A and W, the three calls,
+    # D2H of C, every step
+    e2e = None
+    if rank == 0 or world > 1:
+        a_h = a.cpu().pin_memory()
+        w_h = w.cpu().pin_memory()
+        c_h = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
+        e2e_steps = max(3, min(10, args.steps))
+        for i in range(e2e_steps + 1):
+            if i == 1:
+                torch.cuda.synchronize(dev)
+                s0 = torch.cuda.Event(enable_timing=True)
+                s0.record(stream)
+            a.copy_(a_h, non_blocking=True)
+            w.copy_(w_h, non_blocking=True)
+            step()
+            c_h.copy_(c, non_blocking=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = s0.elapsed_time(s1) / e2e_steps
+        e2e = {"value": round(gemm_flops(M, N, K) * world / (e2e_ms * 1e-3) / 1e12, 2),
+               "unit": "TFLOP/s",
+               "h2d_bytes_per_step": a.numel() * 2 + w.numel() * 2,
+               "d2h_bytes_per_step": c.numel() * 2,
+               "ms_per_step": round(e2e_ms, 4)}
+
+    peaks, peak_src = load_peaks()
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    g_tflops = gemm_flops(M, N, K) / (g_ms * 1e-3) / 1e12
+    qa_gbs = M * K * ACT_BYTES_PER_ELEM / (qa_ms * 1e-3) / 1e9
+    qw_gbs = N * K * W_BYTES_PER_ELEM / (qw_ms * 1e-3) / 1e9
+    traffic = traffic_from_profile()
+    value = gemm_flops(M, N, K) * world / (ms * 1e-3) / 1e12
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3",
+        "data": "synthetic (seeded N(0,1) activations with 0.1% x100 outliers, N(0,0.02) weights)",
+        "config": {"workload": SHAPE.name, "M": M, "N": N, "K": K, "out": "bf16",
+                   "step": "quant_act_1x128 + quant_weight_128x128 + blockscaled_gemm",
+                   "l2": "inputs larger than L2 (A+W BF16 = %.0f MB > 126 MB)"
+                         % ((M + N) * K * 2 / 1e6),
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"kernel": "fp8_blockscaled_gemm", "bound": "tensor",
+                     "achieved": round(g_tflops, 1), "peak": round(fp8_peak, 1),
+                     "unit": "TFLOP/s", "frac": round(g_tflops / fp8_peak, 4),
+                     "traffic": traffic,
+                     "peak_source": f"{peak_src}: 2 x bf16 burst {peaks['bf16_tflops']} TFLOP/s "
+                                    "(nominal fp8/bf16 ratio 4.5/2.25)"},
+        "kernels": {
+            "quant_act_1x128": {"ms": round(qa_ms, 5), "GB/s": round(qa_gbs, 1),
+                                "frac_hbm": round(qa_gbs / peaks["hbm_gbs"], 4)},
+            "quant_weight_128x128": {"ms": round(qw_ms, 5), "GB/s": round(qw_gbs, 1),
+                                     "frac_hbm": round(qw_gbs / peaks["hbm_gbs"], 4)},
+            "blockscaled_gemm": {"ms": round(g_ms, 5), "TFLOP/s": round(g_tflops, 1),
+                                 "frac_fp8_peak": round(g_tflops / fp8_peak, 4)},
+            "hbm_peak_gbs": peaks["hbm_gbs"], "peak_source": peak_src,
+        },
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget_s)
+    return line
+
+
+# --------------------------------------------------------------------------------------
+# The oracle on the host cores (CPU baseline and the reference arm)
+# --------------------------------------------------------------------------------------
+
+def _oracle_sample(rows: int, a_bits, w_bits, threads: int):
+    """The oracle's version of one step restricted to `rows` activation rows: quantize those
+    rows and all of W, then the GEMM of those rows against every weight row. Returns seconds."""
+    from oracle import oracle as O
+    M, K = a_bits.shape
+    N = w_bits.shape[0]
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(threads) as ex:
+        acuts = np.linspace(0, rows, threads + 1).astype(int)
+        aparts = list(ex.map(lambda i: O.quant_act_1x128(a_bits[acuts[i]:acuts[i + 1]]),
+                             range(threads)))
+        nb = (N + 127) // 128
+        wcuts = (np.linspace(0, nb, threads + 1).astype(int) * 128).clip(max=N)
+        wparts = list(ex.map(lambda i: O.quant_weight_128x128(w_bits[wcuts[i]:wcuts[i + 1]]),
+                             range(threads)))
+        qa = np.concatenate([p[0] for p in aparts])
+        sa = np.concatenate([p[1] for p in aparts], axis=1)
+        qw = np.concatenate([p[0] for p in wparts])
+        sw = np.concatenate([p[1] for p in wparts], axis=0)
+        mm, nn = np.meshgrid(np.arange(rows), np.arange(N), indexing="ij")
+        pm, pn = mm.ravel(), nn.ravel()
+        pcuts = np.linspace(0, pm.size, threads + 1).astype(int)
+        list(ex.map(lambda i: O.gemm_points(qa, sa, qw, sw, pm[pcuts[i]:pcuts[i + 1]],
+                                            pn[pcuts[i]:pcuts[i + 1]]), range(threads)))
+    return time.perf_counter() - t0
+
+
+def _host_inputs():
+    a, w = WL.gemm_inputs(SHAPE, "cpu")
+    from oracle import oracle as O
+    O.build()
+    return (a.view(torch.int16).numpy().view(np.uint16),
+            w.view(torch.int16).numpy().view(np.uint16))
+
+
+def _threads():
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def cpu_baseline(budget_s: float = 20.0):
+    a_bits, w_bits = _host_inputs()
+    threads = _threads()
+    N, K = SHAPE.N, SHAPE.K
+    probe_rows = max(1, threads // 4)
+    t = _oracle_sample(probe_rows, a_bits, w_bits, threads)
+    rows = int(max(probe_rows, min(SHAPE.M, probe_rows * budget_s / max(t, 1e-3) * 0.8)))
+    t = _oracle_sample(rows, a_bits, w_bits, threads)
+    value = gemm_flops(rows, N, K) / t / 1e12
+    return {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "seconds": round(t, 3),
+            "sample": f"oracle step on {rows} of {SHAPE.M} activation rows: quantize those rows "
+                      f"and all of W ({N}x{K}), then the FP64 block-scaled GEMM of the "
+                      f"{rows}x{N}x{K} slab; value = 2*{rows}*{N}*{K} / wall time"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    a_bits, w_bits = _host_inputs()
+    threads = _threads()
+    N, K = SHAPE.N, SHAPE.K
+    total_budget = 150.0
+    per_step = total_budget / max(1, args.steps + args.warmup)
+    probe_rows = max(1, threads // 4)
+    t = _oracle_sample(probe_rows, a_bits, w_bits, threads)
+    rows = int(max(1, min(SHAPE.M, probe_rows * per_step / max(t, 1e-3) * 0.8)))
+    for _ in range(args.warmup):
+        _oracle_sample(rows, a_bits, w_bits, threads)
+    times = [_oracle_sample(rows, a_bits, w_bits, threads) for _ in range(args.steps)]
+    sec = sum(times) / len(times)
+    value = gemm_flops(rows, N, K) / sec / 1e12
+    sample = (f"each step: the oracle's quantize + FP64 block-scaled GEMM on {rows} of "
+              f"{SHAPE.M} activation rows against all of W ({N}x{K}); "
+              f"value = 2*{rows}*{N}*{K} / step time")
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(sec * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (same seeded dense workload, generated on the host)",
+        "config": {"workload": SHAPE.name, "M": SHAPE.M, "N": N, "K": K, "out": "f64",
+                   "sample_rows": rows},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the oracle timing on the host cores")
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    rank, world, local_rank = dist_env()
+    if world > 1:
+        backend = "nccl" if (args.impl == "ours" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group(backend)
+    try:
+        if args.impl == "reference":
+            line = run_reference(args, rank, world)
+        else:
+            line = run_ours(args, rank, world, local_rank)
+        if rank == 0 and line is not None:
+            print(json.dumps(line), flush=True)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

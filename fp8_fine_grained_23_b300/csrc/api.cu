@@ -1,0 +1,297 @@
+// api.cu -- the C ABI declared in include/fp8bs.h: argument checks, device checks, TMA
+// descriptors, the per-device error word, and kernel dispatch. Everything is asynchronous on the
+// caller's stream; nothing here synchronizes except fp8bs_last_error().
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "fp8bs.h"
+#include "internal.h"
+
+using namespace fp8bs;
+
+namespace {
+
+constexpr int MAX_DEVICES = 64;
+
+struct DeviceInfo {
+    int checked = 0;      // 0 unknown, 1 sm_103, -1 other
+    int num_sms = 0;
+    int* err = nullptr;   // device error word (allocated on first GEMM call)
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[MAX_DEVICES];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Default spin-wait budget: 2^31 SM cycles, about one second at the B300's clocks.
+long long wait_budget()
+{
+    static long long budget = [] {
+        const char* e = std::getenv("FP8BS_WAIT_BUDGET_CYCLES");
+        long long v = e ? std::atoll(e) : 0;
+        return v > 0 ? v : (1LL << 31);
+    }();
+    return budget;
+}
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// Current device, checked to be compute capability 10.3; fills *info.
+int current_device(DeviceInfo** info)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) {
+        cudaGetLastError();
+        return FP8BS_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (d.checked == 0) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return FP8BS_ERR_CUDA;
+        }
+        d.checked = (major == 10 && minor == 3) ? 1 : -1;
+        d.num_sms = sms;
+    }
+    if (d.checked != 1) return FP8BS_ERR_UNSUPPORTED_DEVICE;
+    *info = &d;
+    return FP8BS_OK;
+}
+
+int ensure_error_word(DeviceInfo* d)
+{
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (d->err) return FP8BS_OK;
+    int* p = nullptr;
+    if (cudaMalloc(&p, sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8BS_ERR_CUDA;
+    }
+    if (cudaMemset(p, 0, sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(p);
+        return FP8BS_ERR_CUDA;
+    }
+    d->err = p;
+    return FP8BS_OK;
+}
+
+int ensure_encoder()
+{
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_encode) return FP8BS_OK;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr) {
+        cudaGetLastError();
+        return FP8BS_ERR_CUDA;
+    }
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return FP8BS_OK;
+}
+
+// 2-D map over a row-major byte matrix [rows][cols] (row stride `ld` bytes), loaded in boxes of
+// 128 bytes x box_rows rows with the 128-byte swizzle; out-of-range rows read as zero.
+int make_code_map(CUtensorMap* map, const void* base, int64_t cols, int64_t rows, int64_t ld,
+                  int box_rows)
+{
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld)};
+    const cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FP8BS_OK : FP8BS_ERR_CUDA;
+}
+
+int check_quant_args(const void* in, int64_t rows, int64_t K, int64_t ld_in, const void* q,
+                     int64_t ldq, const void* scales)
+{
+    if (rows < 0 || K <= 0 || K % 128 != 0 || ld_in < K || ldq < K) return FP8BS_ERR_INVALID_ARG;
+    if (rows > INT32_MAX || K > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
+    if (rows == 0) return FP8BS_OK;
+    if (!in || !q || !scales) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned16(in) || !aligned16(q) || !aligned4(scales) || ld_in % 8 != 0 || ldq % 16 != 0)
+        return FP8BS_ERR_MISALIGNED;
+    return FP8BS_OK;
+}
+
+int check_gemm_args(const void* a_q, const void* a_s, const void* w_q, const void* w_s,
+                    int64_t rows, int64_t N, int64_t K, const void* c, int64_t ldc, int out_dtype)
+{
+    if (out_dtype != FP8BS_OUT_BF16 && out_dtype != FP8BS_OUT_F32) return FP8BS_ERR_INVALID_ARG;
+    if (rows < 0 || N <= 0 || N % 16 != 0 || K <= 0 || K % 128 != 0 || ldc < N)
+        return FP8BS_ERR_INVALID_ARG;
+    if (rows > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
+    if (rows == 0) return FP8BS_OK;
+    if (!a_q || !a_s || !w_q || !w_s || !c) return FP8BS_ERR_INVALID_ARG;
+    const int64_t elem = out_dtype == FP8BS_OUT_F32 ? 4 : 2;
+    if (!aligned16(a_q) || !aligned16(w_q) || !aligned16(c) || !aligned4(a_s) || !aligned4(w_s) ||
+        (ldc * elem) % 16 != 0)
+        return FP8BS_ERR_MISALIGNED;
+    return FP8BS_OK;
+}
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? FP8BS_OK : FP8BS_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int fp8_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, int64_t ldq,
+                        float* scales, fp8bs_stream_t stream)
+{
+    int st = check_quant_args(x, M, K, ldx, q, ldq, scales);
+    if (st != FP8BS_OK || M == 0) return st;
+    DeviceInfo* d = nullptr;
+    if ((st = current_device(&d)) != FP8BS_OK) return st;
+    return cuda_status(launch_quant_act(x, M, K, ldx, q, ldq, scales, d->num_sms,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fp8_quant_weight_128x128(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
+                             int64_t ldq, float* scales, fp8bs_stream_t stream)
+{
+    int st = check_quant_args(w, N, K, ldw, q, ldq, scales);
+    if (st != FP8BS_OK || N == 0) return st;
+    if ((N + 127) / 128 > 65535) return FP8BS_ERR_INVALID_ARG;   // grid.y limit
+    DeviceInfo* d = nullptr;
+    if ((st = current_device(&d)) != FP8BS_OK) return st;
+    return cuda_status(
+        launch_quant_weight(w, N, K, ldw, q, ldq, scales, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fp8_blockscaled_gemm(const uint8_t* a_q, const float* a_s, const uint8_t* w_q,
+                         const float* w_s, int64_t M, int64_t N, int64_t K, void* c, int64_t ldc,
+                         int out_dtype, fp8bs_stream_t stream)
+{
+    int st = check_gemm_args(a_q, a_s, w_q, w_s, M, N, K, c, ldc, out_dtype);
+    if (st != FP8BS_OK || M == 0) return st;
+    DeviceInfo* d = nullptr;
+    if ((st = current_device(&d)) != FP8BS_OK) return st;
+    if ((st = ensure_error_word(d)) != FP8BS_OK) return st;
+    if ((st = ensure_encoder()) != FP8BS_OK) return st;
+
+    CUtensorMap ma, mb;
+    if ((st = make_code_map(&ma, a_q, K, M, K, GEMM_BM)) != FP8BS_OK) return st;
+    if ((st = make_code_map(&mb, w_q, K, N, K, GEMM_BN)) != FP8BS_OK) return st;
+
+    GemmArgs args{};
+    args.a_s = a_s;
+    args.w_s = w_s;
+    args.c = c;
+    args.ldc = ldc;
+    args.rows = M;
+    args.N = static_cast<int>(N);
+    args.KB = static_cast<int>(K / 128);
+    args.NB = static_cast<int>((N + 127) / 128);
+    args.NT = static_cast<int>((N + GEMM_BN - 1) / GEMM_BN);
+    args.MT = static_cast<int>((M + GEMM_BM - 1) / GEMM_BM);
+    const int64_t tiles = static_cast<int64_t>(args.MT) * args.NT;
+    if (tiles > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
+    args.num_tiles = static_cast<int>(tiles);
+    args.offsets = nullptr;
+    args.G = 1;
+    args.err = d->err;
+    args.budget = wait_budget();
+    const int grid = static_cast<int>(tiles < d->num_sms ? tiles : d->num_sms);
+    return cuda_status(launch_gemm(ma, mb, args, false, out_dtype == FP8BS_OUT_F32, grid,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fp8_blockscaled_grouped_gemm(const uint8_t* a_q, const float* a_s, const uint8_t* w_q,
+                                 const float* w_s, const int32_t* group_offsets, int64_t G,
+                                 int64_t R, int64_t N, int64_t K, void* c, int64_t ldc,
+                                 int out_dtype, fp8bs_stream_t stream)
+{
+    if (G < 1 || G > GEMM_MAX_GROUPS) return FP8BS_ERR_INVALID_ARG;
+    int st = check_gemm_args(a_q, a_s, w_q, w_s, R, N, K, c, ldc, out_dtype);
+    if (st != FP8BS_OK || R == 0) return st;
+    if (!group_offsets) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned4(group_offsets)) return FP8BS_ERR_MISALIGNED;
+    if (G * N > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
+    DeviceInfo* d = nullptr;
+    if ((st = current_device(&d)) != FP8BS_OK) return st;
+    if ((st = ensure_error_word(d)) != FP8BS_OK) return st;
+    if ((st = ensure_encoder()) != FP8BS_OK) return st;
+
+    CUtensorMap ma, mb;
+    if ((st = make_code_map(&ma, a_q, K, R, K, GEMM_BM)) != FP8BS_OK) return st;
+    if ((st = make_code_map(&mb, w_q, K, G * N, K, GEMM_BN)) != FP8BS_OK) return st;
+
+    GemmArgs args{};
+    args.a_s = a_s;
+    args.w_s = w_s;
+    args.c = c;
+    args.ldc = ldc;
+    args.rows = R;
+    args.N = static_cast<int>(N);
+    args.KB = static_cast<int>(K / 128);
+    args.NB = static_cast<int>((N + 127) / 128);
+    args.NT = static_cast<int>((N + GEMM_BN - 1) / GEMM_BN);
+    args.MT = 0;
+    args.num_tiles = 0;
+    args.offsets = group_offsets;
+    args.G = static_cast<int>(G);
+    args.err = d->err;
+    args.budget = wait_budget();
+    // At most ceil(R/128) + G m-tiles exist across the groups; the exact count is formed on the
+    // device from the offsets, and CTAs without a tile exit at once.
+    const int64_t bound = ((R + GEMM_BM - 1) / GEMM_BM + G) * args.NT;
+    if (bound > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
+    const int grid = static_cast<int>(bound < d->num_sms ? bound : d->num_sms);
+    return cuda_status(launch_gemm(ma, mb, args, true, out_dtype == FP8BS_OUT_F32, grid,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+const char* fp8bs_status_string(int status)
+{
+    switch (status) {
+        case FP8BS_OK: return "FP8BS_OK";
+        case FP8BS_ERR_INVALID_ARG: return "FP8BS_ERR_INVALID_ARG";
+        case FP8BS_ERR_MISALIGNED: return "FP8BS_ERR_MISALIGNED";
+        case FP8BS_ERR_UNSUPPORTED_DEVICE: return "FP8BS_ERR_UNSUPPORTED_DEVICE";
+        case FP8BS_ERR_CUDA: return "FP8BS_ERR_CUDA";
+        case FP8BS_ERR_TIMEOUT: return "FP8BS_ERR_TIMEOUT";
+        default: return "FP8BS_ERR_UNKNOWN";
+    }
+}
+
+int fp8bs_last_error(fp8bs_stream_t stream)
+{
+    DeviceInfo* d = nullptr;
+    int st = current_device(&d);
+    if (st != FP8BS_OK) return st;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8BS_ERR_CUDA;
+    }
+    if (!d->err) return FP8BS_OK;
+    int h = 0;
+    if (cudaMemcpy(&h, d->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8BS_ERR_CUDA;
+    }
+    if (h == DEV_OK) return FP8BS_OK;
+    if (cudaMemset(d->err, 0, sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8BS_ERR_CUDA;
+    }
+    return FP8BS_ERR_TIMEOUT;
+}
+
+}  // extern "C"

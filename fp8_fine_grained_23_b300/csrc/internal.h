@@ -1,0 +1,55 @@
+// internal.h -- launchers shared between the C-ABI layer (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace fp8bs {
+
+constexpr int QUANT_THREADS = 256;
+
+// GEMM tiling: one CTA computes a 128 x GEMM_BN tile of C; each pipeline stage holds one
+// 128-wide K block (the quantization block) of A and W.
+constexpr int GEMM_BM = 128;
+constexpr int GEMM_BN = 256;
+constexpr int GEMM_BK = 128;
+constexpr int GEMM_MAX_GROUPS = 1024;
+
+// Device error word codes (the first error of a launch wins).
+enum DeviceError : int {
+    DEV_OK = 0,
+    DEV_TIMEOUT_PRODUCER = 1,   // TMA producer: a smem stage never became free
+    DEV_TIMEOUT_MMA_TMEM = 2,   // MMA issuer: a TMEM accumulator buffer never drained
+    DEV_TIMEOUT_MMA_FULL = 3,   // MMA issuer: a smem stage never filled
+    DEV_TIMEOUT_EPILOGUE = 4,   // epilogue: a K-block partial never arrived
+    DEV_TIMEOUT_DRAIN = 5,      // clean-up: in-flight copies or MMAs did not finish
+};
+
+struct GemmArgs {
+    const float* a_s;         // [K/128][rows]
+    const float* w_s;         // [G][ceil(N/128)][K/128]
+    void* c;                  // [rows][ldc]
+    int64_t ldc;
+    int64_t rows;             // M (dense) or R (grouped)
+    int N;
+    int KB;                   // K / 128
+    int NB;                   // ceil(N / 128)
+    int NT;                   // ceil(N / GEMM_BN)
+    int MT;                   // dense: ceil(M / 128)
+    int num_tiles;            // dense: MT * NT (grouped: computed on the device)
+    const int32_t* offsets;   // grouped: [G+1] on the device
+    int G;
+    int* err;                 // device error word
+    long long budget;         // spin-wait budget in SM clock cycles
+};
+
+cudaError_t launch_quant_act(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
+                             int64_t ldq, float* scales, int num_sms, cudaStream_t stream);
+cudaError_t launch_quant_weight(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
+                                int64_t ldq, float* scales, cudaStream_t stream);
+cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args,
+                        bool grouped, bool out_f32, int grid, cudaStream_t stream);
+size_t gemm_smem_bytes(bool grouped, int G);
+
+}  // namespace fp8bs

@@ -1,0 +1,158 @@
+"""Python binding of libfp8bs (the C ABI in ``include/fp8bs.h``).
+
+Argument marshalling only: every step of the quantize + GEMM path runs in the library's CUDA
+kernels. PyTorch supplies device memory and the current stream. Importing this module fails
+loudly when ``libfp8bs.so`` has not been built (``python -m fp8_fine_grained_23_b300.build``);
+there is no fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfp8bs.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"libfp8bs.so is not built ({LIB_PATH}); run `python -m fp8_fine_grained_23_b300.build`")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+_i64, _p, _int = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+lib.fp8_quant_act_1x128.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p, _p]
+lib.fp8_quant_weight_128x128.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p, _p]
+lib.fp8_blockscaled_gemm.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, _p, _i64, _int, _p]
+lib.fp8_blockscaled_grouped_gemm.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _p,
+                                             _i64, _int, _p]
+lib.fp8bs_status_string.argtypes = [_int]
+lib.fp8bs_status_string.restype = ctypes.c_char_p
+lib.fp8bs_last_error.argtypes = [_p]
+for _f in (lib.fp8_quant_act_1x128, lib.fp8_quant_weight_128x128, lib.fp8_blockscaled_gemm,
+           lib.fp8_blockscaled_grouped_gemm, lib.fp8bs_last_error):
+    _f.restype = _int
+
+FP8BS_OK = 0
+FP8BS_ERR_INVALID_ARG = -1
+FP8BS_ERR_MISALIGNED = -2
+FP8BS_ERR_UNSUPPORTED_DEVICE = -3
+FP8BS_ERR_CUDA = -4
+FP8BS_ERR_TIMEOUT = -5
+FP8BS_OUT_BF16 = 0
+FP8BS_OUT_F32 = 1
+
+
+class Fp8bsError(RuntimeError):
+    def __init__(self, call: str, status: int):
+        self.status = status
+        super().__init__(f"{call} failed: {fp8bs_status_string(status)} ({status})")
+
+
+def fp8bs_status_string(status: int) -> str:
+    return lib.fp8bs_status_string(status).decode()
+
+
+def _check(call: str, status: int) -> None:
+    if status != FP8BS_OK:
+        raise Fp8bsError(call, status)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _rows_ld(t: torch.Tensor, name: str) -> tuple[int, int]:
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be a 2-D tensor with unit column stride")
+    return t.shape[0], t.stride(0)
+
+
+def fp8_quant_act_1x128(x: torch.Tensor, q: torch.Tensor | None = None,
+                        scales: torch.Tensor | None = None, stream=None):
+    """E4M3 codes [M][K] (uint8) and FP32 scales [K/128][M] of BF16 activations x [M][K]."""
+    if x.dtype != torch.bfloat16:
+        raise TypeError("x must be bfloat16")
+    M, ldx = _rows_ld(x, "x")
+    K = x.shape[1]
+    if q is None:
+        q = torch.empty(M, K, dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(K // 128, M, dtype=torch.float32, device=x.device)
+    _, ldq = _rows_ld(q, "q")
+    _check("fp8_quant_act_1x128",
+           lib.fp8_quant_act_1x128(x.data_ptr(), M, K, ldx, q.data_ptr(), ldq, scales.data_ptr(),
+                                   _stream(stream)))
+    return q, scales
+
+
+def fp8_quant_weight_128x128(w: torch.Tensor, q: torch.Tensor | None = None,
+                             scales: torch.Tensor | None = None, stream=None):
+    """E4M3 codes [N][K] and FP32 scales [ceil(N/128)][K/128] of BF16 weights w [N][K]."""
+    if w.dtype != torch.bfloat16:
+        raise TypeError("w must be bfloat16")
+    N, ldw = _rows_ld(w, "w")
+    K = w.shape[1]
+    if q is None:
+        q = torch.empty(N, K, dtype=torch.uint8, device=w.device)
+    if scales is None:
+        scales = torch.empty((N + 127) // 128, K // 128, dtype=torch.float32, device=w.device)
+    _, ldq = _rows_ld(q, "q")
+    _check("fp8_quant_weight_128x128",
+           lib.fp8_quant_weight_128x128(w.data_ptr(), N, K, ldw, q.data_ptr(), ldq,
+                                        scales.data_ptr(), _stream(stream)))
+    return q, scales
+
+
+def _out_code(dtype) -> int:
+    if dtype == torch.bfloat16:
+        return FP8BS_OUT_BF16
+    if dtype == torch.float32:
+        return FP8BS_OUT_F32
+    raise TypeError("output dtype must be bfloat16 or float32")
+
+
+def fp8_blockscaled_gemm(a_q: torch.Tensor, a_s: torch.Tensor, w_q: torch.Tensor,
+                         w_s: torch.Tensor, out: torch.Tensor | None = None,
+                         out_dtype=torch.bfloat16, stream=None) -> torch.Tensor:
+    """C [M][N] = A W^T with per-(1x128) activation and per-(128x128) weight scales."""
+    M, K = a_q.shape
+    N = w_q.shape[0]
+    if out is None:
+        out = torch.empty(M, N, dtype=out_dtype, device=a_q.device)
+    _, ldc = _rows_ld(out, "out")
+    _check("fp8_blockscaled_gemm",
+           lib.fp8_blockscaled_gemm(a_q.data_ptr(), a_s.data_ptr(), w_q.data_ptr(),
+                                    w_s.data_ptr(), M, N, K, out.data_ptr(), ldc,
+                                    _out_code(out.dtype), _stream(stream)))
+    return out
+
+
+def fp8_blockscaled_grouped_gemm(a_q: torch.Tensor, a_s: torch.Tensor, w_q: torch.Tensor,
+                                 w_s: torch.Tensor, group_offsets: torch.Tensor,
+                                 out: torch.Tensor | None = None, out_dtype=torch.bfloat16,
+                                 stream=None) -> torch.Tensor:
+    """Per-group C rows: rows [off[g], off[g+1]) of A use weights w_q[g] ([G][N][K])."""
+    R, K = a_q.shape
+    G, N = w_q.shape[0], w_q.shape[1]
+    if group_offsets.dtype != torch.int32 or group_offsets.numel() != G + 1:
+        raise ValueError("group_offsets must be int32 with G + 1 entries")
+    if out is None:
+        out = torch.empty(R, N, dtype=out_dtype, device=a_q.device)
+    _, ldc = _rows_ld(out, "out")
+    _check("fp8_blockscaled_grouped_gemm",
+           lib.fp8_blockscaled_grouped_gemm(a_q.data_ptr(), a_s.data_ptr(), w_q.data_ptr(),
+                                            w_s.data_ptr(), group_offsets.data_ptr(), G, R, N, K,
+                                            out.data_ptr(), ldc, _out_code(out.dtype),
+                                            _stream(stream)))
+    return out
+
+
+def fp8bs_last_error(stream=None) -> int:
+    """Synchronize the stream; return (and clear) the device error word's status."""
+    return lib.fp8bs_last_error(_stream(stream))

@@ -1,0 +1,145 @@
+/*
+ * fp8bs.h -- C ABI of libfp8bs: fine-grained FP8 (E4M3) quantization and block-scaled FP8
+ * GEMM for NVIDIA B300 (sm_103a).
+ *
+ * The operations follow the DeepSeek-V3 FP8 training write-ups:
+ *   [codingmall]  "Bạn có thể giải thích vai trò của độ chính xác FP8 trong quá trình đào tạo
+ *                 của DeepSeek-V3" (codingmall.com), sections "Định lượng hạt mịn",
+ *                 "Định lượng trực tuyến", "Tăng độ chính xác tích lũy", "Định dạng E4M3 hợp nhất";
+ *   [dtcms]       DeepSeek-V3 overview (dtcms.com), section 三 "FP8混合精度训练", parts 1-3;
+ *   [risenshine]  DeepSeek training-algorithm article (risenshineclean.com), section 三;
+ *   [MoE]         dtcms.com section 一.2 "DeepSeekMoE架构" and risenshineclean.com section 二
+ *                 (256 routed experts, each token routed to 8).
+ * The pages define no interface; this one is the project's own.
+ *
+ * Conventions shared by every call
+ *  - All tensors are row-major and live in DEVICE memory owned by the caller. The library
+ *    never allocates per call; the first call on a device allocates one 4-byte error word that
+ *    lives until the process exits (make that first call outside CUDA graph capture).
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy default stream) and
+ *    never synchronize. Every output buffer is fully overwritten.
+ *  - E4M3 codes are OCP E4M3FN bytes (bias 7, largest finite 448, no infinities).
+ *  - Quantization of a tile with amax = max|x| > 0: s = amax / 448 (IEEE FP32 division),
+ *    code = E4M3_rne_satfinite(x * (448 / amax)), one FP32 multiply per element; for
+ *    amax < 2^-64 the same value is formed as (x * 2^64) * (448 / (amax * 2^64)). A tile with
+ *    amax == 0 gets s = 1 and all codes 0x00. Dequantized value: decode(code) * s.
+ *  - Argument errors are detected on the host before anything is launched and return
+ *    FP8BS_ERR_INVALID_ARG or FP8BS_ERR_MISALIGNED; a device that is not sm_103 returns
+ *    FP8BS_ERR_UNSUPPORTED_DEVICE; a CUDA launch error returns FP8BS_ERR_CUDA. Errors raised
+ *    inside a running kernel (a pipeline wait that ran past its time budget) are reported
+ *    later by fp8bs_last_error().
+ *  - Calls are thread-safe. Non-finite inputs are outside the contract (no hang; the result
+ *    is unspecified).
+ */
+#ifndef FP8BS_H
+#define FP8BS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+struct CUstream_st;
+typedef struct CUstream_st *fp8bs_stream_t;
+
+enum fp8bs_status {
+    FP8BS_OK = 0,
+    FP8BS_ERR_INVALID_ARG = -1,        /* shape, leading dimension, null pointer, dtype */
+    FP8BS_ERR_MISALIGNED = -2,         /* a pointer or leading dimension breaks 16-byte alignment */
+    FP8BS_ERR_UNSUPPORTED_DEVICE = -3, /* the current device is not compute capability 10.3 */
+    FP8BS_ERR_CUDA = -4,               /* a CUDA runtime/driver call failed */
+    FP8BS_ERR_TIMEOUT = -5             /* a kernel's pipeline wait ran past its budget */
+};
+
+enum fp8bs_out_dtype {
+    FP8BS_OUT_BF16 = 0,
+    FP8BS_OUT_F32 = 1
+};
+
+/*
+ * Online 1x128 activation quantization ([codingmall] "Định lượng hạt mịn" and "Định lượng
+ * trực tuyến"; [risenshine] 三: one token by 128 channels per tile).
+ *   x       BF16 [M][ldx], the first K columns are read.
+ *   q       E4M3 codes [M][ldq], the first K columns are written.
+ *   scales  FP32 [K/128][M] (M contiguous): scales[kb*M + m] is the scale of row m, columns
+ *           [128 kb, 128 kb + 128).
+ * Requires M >= 0 (M == 0 is a no-op), K > 0, K % 128 == 0, ldx >= K, ldq >= K,
+ * ldx % 8 == 0, ldq % 16 == 0, x and q 16-byte aligned, scales 4-byte aligned.
+ */
+int fp8_quant_act_1x128(const void *x, int64_t M, int64_t K, int64_t ldx,
+                        uint8_t *q, int64_t ldq, float *scales, fp8bs_stream_t stream);
+
+/*
+ * Online 128x128 weight-block quantization ([codingmall] "Định lượng hạt mịn"; [dtcms] 三.2).
+ *   w       BF16 [N][ldw] (row n is output channel n), the first K columns are read.
+ *   q       E4M3 codes [N][ldq].
+ *   scales  FP32 [ceil(N/128)][K/128]: scales[nb*(K/128) + kb] covers rows
+ *           [128 nb, min(N, 128 nb + 128)) and columns [128 kb, 128 kb + 128). A last, partial
+ *           row block takes its amax over its real rows only.
+ * Stacked per-expert weights [E][N][K] with N % 128 == 0 may be passed as one [E*N][K]
+ * matrix; the scales then come out as [E][N/128][K/128].
+ * Requires N >= 0 (N == 0 is a no-op), K > 0, K % 128 == 0, ldw >= K, ldq >= K,
+ * ldw % 8 == 0, ldq % 16 == 0, w and q 16-byte aligned, scales 4-byte aligned.
+ */
+int fp8_quant_weight_128x128(const void *w, int64_t N, int64_t K, int64_t ldw,
+                             uint8_t *q, int64_t ldq, float *scales, fp8bs_stream_t stream);
+
+/*
+ * Block-scaled FP8 GEMM, C = A W^T ([dtcms] 三.1: FP8 inputs, BF16 or FP32 output;
+ * [codingmall] "Tăng độ chính xác tích lũy": partial sums promoted to FP32 at intervals).
+ *   C[m][n] = sum_kb  a_s[kb*M + m] * w_s[(n/128)*(K/128) + kb] * P[m][n][kb],
+ *   P[m][n][kb] = sum over k in [128 kb, 128 kb + 128) of decode(a_q[m][k]) * decode(w_q[n][k]).
+ * Each P is formed by the tensor cores in FP32 and promoted once per 128-wide K block: it is
+ * multiplied by the FP32 product of its two scales and added to an FP32 accumulator with one
+ * fused multiply-add. The accumulation order over K blocks is increasing kb.
+ *   a_q  E4M3 [M][K] (contiguous rows), a_s FP32 [K/128][M]   (fp8_quant_act_1x128 layout)
+ *   w_q  E4M3 [N][K] (contiguous rows), w_s FP32 [ceil(N/128)][K/128] (weight-quantizer layout)
+ *   c    [M][ldc] of BF16 (out_dtype FP8BS_OUT_BF16, round to nearest even) or FP32.
+ * Requires M >= 0 (M == 0 is a no-op), N > 0, N % 16 == 0, K > 0, K % 128 == 0,
+ * M, N <= 2^31 - 1, ldc >= N, ldc * sizeof(out) % 16 == 0, a_q, w_q and c 16-byte aligned,
+ * a_s and w_s 4-byte aligned.
+ */
+int fp8_blockscaled_gemm(const uint8_t *a_q, const float *a_s,
+                         const uint8_t *w_q, const float *w_s,
+                         int64_t M, int64_t N, int64_t K,
+                         void *c, int64_t ldc, int out_dtype, fp8bs_stream_t stream);
+
+/*
+ * Grouped block-scaled FP8 GEMM for routed MoE experts ([MoE]; the pages name no grouped
+ * kernel, this is the dense GEMM above applied per expert):
+ *   for every group g and row r in [off[g], off[g+1]):
+ *     C[r][n] = sum_kb a_s[kb*R + r] * w_s[g][n/128][kb] * P_g[r][n][kb]
+ *   with P_g formed from a_q[r] and expert g's codes w_q[g][n].
+ *   a_q            E4M3 [R][K], rows sorted by group; a_s FP32 [K/128][R]
+ *   w_q            E4M3 [G][N][K]; w_s FP32 [G][ceil(N/128)][K/128]
+ *   group_offsets  DEVICE int32 [G+1], off[0] = 0, non-decreasing, off[G] = R. The kernel
+ *                  reads it on the device, so no host synchronization is needed. Offsets
+ *                  outside [0, R] or decreasing are outside the contract (no hang; the rows
+ *                  written are unspecified).
+ *   c              [R][ldc] BF16 or FP32.
+ * Requires G in [1, 4096], R >= 0 (R == 0 is a no-op), plus the dense call's rules for N, K,
+ * ldc and alignment. Empty groups are allowed.
+ */
+int fp8_blockscaled_grouped_gemm(const uint8_t *a_q, const float *a_s,
+                                 const uint8_t *w_q, const float *w_s,
+                                 const int32_t *group_offsets, int64_t G, int64_t R,
+                                 int64_t N, int64_t K, void *c, int64_t ldc, int out_dtype,
+                                 fp8bs_stream_t stream);
+
+/* Human-readable name of a status code. The string is static. */
+const char *fp8bs_status_string(int status);
+
+/*
+ * Synchronizes `stream`, then reads and clears the current device's error word, which the
+ * GEMM kernels set when a pipeline wait runs past its budget (they then stop, drain their
+ * in-flight copies and return). Returns FP8BS_OK, FP8BS_ERR_TIMEOUT or FP8BS_ERR_CUDA.
+ */
+int fp8bs_last_error(fp8bs_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8BS_H */

@@ -1,0 +1,99 @@
+"""Shared pieces of the GPU parity tests: the library fixture and oracle runners that split big
+inputs into row slabs over host threads (the oracle's C calls release the GIL)."""
+from __future__ import annotations
+
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle as O
+from tests.helpers import bits_of, gemm_tolerance
+
+THREADS = max(1, min(32, os.cpu_count() or 1))
+
+
+@pytest.fixture(scope="session")
+def F():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from fp8_fine_grained_23_b300 import build
+    build.build()
+    from fp8_fine_grained_23_b300 import fp8bs
+    return fp8bs
+
+
+def oracle_quant_act(x_bits: np.ndarray):
+    """Oracle 1x128 quantization of [M][K] BF16 bits, row slabs on host threads."""
+    M = x_bits.shape[0]
+    if M < 4096:
+        return O.quant_act_1x128(x_bits)
+    cuts = np.linspace(0, M, THREADS + 1).astype(int)
+    with ThreadPoolExecutor(THREADS) as ex:
+        parts = list(ex.map(lambda i: O.quant_act_1x128(x_bits[cuts[i]:cuts[i + 1]]),
+                            range(THREADS)))
+    return np.concatenate([p[0] for p in parts]), np.concatenate([p[1] for p in parts], axis=1)
+
+
+def oracle_quant_weight(w_bits: np.ndarray):
+    """Oracle 128x128 quantization; slabs are whole 128-row blocks."""
+    N = w_bits.shape[0]
+    nb = (N + 127) // 128
+    if nb < 16:
+        return O.quant_weight_128x128(w_bits)
+    cuts = np.linspace(0, nb, min(THREADS, nb) + 1).astype(int) * 128
+    cuts[-1] = N
+    with ThreadPoolExecutor(THREADS) as ex:
+        parts = list(ex.map(lambda i: O.quant_weight_128x128(w_bits[cuts[i]:cuts[i + 1]]),
+                            range(len(cuts) - 1)))
+    return np.concatenate([p[0] for p in parts]), np.concatenate([p[1] for p in parts], axis=0)
+
+
+def oracle_points(aq, a_s, wq, w_s, pm, pn):
+    """Oracle GEMM elements at (pm[i], pn[i]) split over host threads."""
+    n = pm.size
+    cuts = np.linspace(0, n, THREADS + 1).astype(int)
+    with ThreadPoolExecutor(THREADS) as ex:
+        parts = list(ex.map(
+            lambda i: O.gemm_points(aq, a_s, wq, w_s, pm[cuts[i]:cuts[i + 1]],
+                                    pn[cuts[i]:cuts[i + 1]]), range(THREADS)))
+    return np.concatenate([p[0] for p in parts]), np.concatenate([p[1] for p in parts])
+
+
+def assert_codes_equal(q_gpu: torch.Tensor, q_orc: np.ndarray):
+    g = q_gpu.cpu().numpy()
+    if not np.array_equal(g, q_orc):
+        bad = np.argwhere(g != q_orc)
+        i = tuple(bad[0])
+        raise AssertionError(f"{len(bad)} codes differ; first at {i}: gpu {g[i]:#04x} "
+                             f"oracle {q_orc[i]:#04x}")
+
+
+def assert_scales_equal(s_gpu: torch.Tensor, s_orc: np.ndarray):
+    g = s_gpu.cpu().numpy().view(np.uint32)
+    o = np.ascontiguousarray(s_orc).view(np.uint32)
+    if not np.array_equal(g, o):
+        bad = np.argwhere(g != o)
+        i = tuple(bad[0])
+        raise AssertionError(f"{len(bad)} scales differ; first at {i}: gpu "
+                             f"{g[i].view(np.float32)!r} oracle {o[i].view(np.float32)!r}")
+
+
+def assert_within_tolerance(c_gpu: np.ndarray, c64: np.ndarray, cabs: np.ndarray, out_dtype: str,
+                            what: str = ""):
+    tol = gemm_tolerance(c64, cabs, out_dtype)
+    err = np.abs(c_gpu.astype(np.float64) - c64)
+    bad = err > tol
+    if bad.any() or not np.isfinite(c_gpu).all():
+        i = np.argmax(err - tol)
+        raise AssertionError(
+            f"{what}: {int(bad.sum())} of {bad.size} outside |gpu-oracle| <= 1e-5*sum|ab| + 1 ulp; "
+            f"worst index {i}: gpu {c_gpu.ravel()[i]!r} oracle {c64.ravel()[i]!r} "
+            f"tol {tol.ravel()[i]!r}")
+    return float((err / np.maximum(cabs, 1e-300)).max())
+
+
+def gpu_bits_pair(a: torch.Tensor, w: torch.Tensor):
+    return bits_of(a), bits_of(w)
