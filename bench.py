@@ -339,13 +339,24 @@ def _threads():
         return max(1, os.cpu_count() or 1)
 
 
+def _calibrate_rows(a_bits, w_bits, threads, budget_s):
+    """Rows of the oracle sample that take about budget_s seconds: two probes give the fixed
+    cost (quantizing W) and the cost per activation row."""
+    r1 = threads
+    t1 = _oracle_sample(r1, a_bits, w_bits, threads)
+    r2 = 3 * threads
+    t2 = _oracle_sample(r2, a_bits, w_bits, threads)
+    per_row = max((t2 - t1) / (r2 - r1), 1e-6)
+    fixed = max(t1 - r1 * per_row, 0.0)
+    rows = int((budget_s - fixed) / per_row)
+    return max(1, min(SHAPE.M, rows))
+
+
 def cpu_baseline(budget_s: float = 20.0):
     a_bits, w_bits = _host_inputs()
     threads = _threads()
     N, K = SHAPE.N, SHAPE.K
-    probe_rows = max(1, threads // 4)
-    t = _oracle_sample(probe_rows, a_bits, w_bits, threads)
-    rows = int(max(probe_rows, min(SHAPE.M, probe_rows * budget_s / max(t, 1e-3) * 0.8)))
+    rows = _calibrate_rows(a_bits, w_bits, threads, budget_s)
     t = _oracle_sample(rows, a_bits, w_bits, threads)
     value = gemm_flops(rows, N, K) / t / 1e12
     return {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
@@ -362,10 +373,8 @@ def run_reference(args, rank, world):
     threads = _threads()
     N, K = SHAPE.N, SHAPE.K
     total_budget = 150.0
-    per_step = total_budget / max(1, args.steps + args.warmup)
-    probe_rows = max(1, threads // 4)
-    t = _oracle_sample(probe_rows, a_bits, w_bits, threads)
-    rows = int(max(1, min(SHAPE.M, probe_rows * per_step / max(t, 1e-3) * 0.8)))
+    per_step = max(0.5, total_budget / max(1, args.steps + args.warmup))
+    rows = _calibrate_rows(a_bits, w_bits, threads, per_step)
     for _ in range(args.warmup):
         _oracle_sample(rows, a_bits, w_bits, threads)
     times = [_oracle_sample(rows, a_bits, w_bits, threads) for _ in range(args.steps)]
@@ -400,7 +409,7 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true",

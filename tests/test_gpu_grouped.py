@@ -22,12 +22,14 @@ def run_grouped(F, a, ws, counts, out_dtype):
     G, N, K = len(ws), ws[0].shape[0], ws[0].shape[1]
     off = W.synthetic_offsets(counts)
     ag = a.cuda()
-    wg = torch.stack(ws).cuda()
     aq, a_s = F.fp8_quant_act_1x128(ag)
-    wq, w_s = F.fp8_quant_weight_128x128(wg.view(G * N, K))
+    # per-expert quantization (a stacked [G*N][K] call needs N % 128 == 0)
+    wq = torch.empty(G, N, K, dtype=torch.uint8, device="cuda")
+    w_s = torch.empty(G, (N + 127) // 128, K // 128, dtype=torch.float32, device="cuda")
+    for g_, w_ in enumerate(ws):
+        F.fp8_quant_weight_128x128(w_.cuda(), wq[g_], w_s[g_])
     offs = torch.from_numpy(off).cuda()
-    c = F.fp8_blockscaled_grouped_gemm(aq, a_s, wq.view(G, N, K), w_s.view(G, -1, K // 128),
-                                       offs, out_dtype=out_dtype)
+    c = F.fp8_blockscaled_grouped_gemm(aq, a_s, wq, w_s, offs, out_dtype=out_dtype)
     assert F.fp8bs_last_error() == F.FP8BS_OK
     return off, aq, a_s, wq, w_s, c
 
