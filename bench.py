@@ -63,6 +63,17 @@ def gemm_flops(M, N, K):
     return 2.0 * M * N * K
 
 
+def reduce_max(values, device=None):
+    """Element-wise maximum of `values` over all ranks (the slowest rank sets the time)."""
+    t = torch.tensor(values, dtype=torch.float64)
+    dist = torch.distributed
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        if dist.get_backend() == "nccl":
+            t = t.to(device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.cpu().tolist()
+
+
 # --------------------------------------------------------------------------------------
 # Clock sampling during the timed region
 # --------------------------------------------------------------------------------------
@@ -209,39 +220,31 @@ def run_ours(args, rank, world, local_rank):
 
     ms = t0.elapsed_time(t1) / args.steps
     k_ms = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in events) for j in range(3)]
-    t = torch.tensor([ms] + k_ms, dtype=torch.float64)
-    if world > 1:
-        tt = t.to(dev) if torch.distributed.get_backend() == "nccl" else t
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        t = tt.cpu()
-    ms, qa_ms, qw_ms, g_ms = t.tolist()
+    ms, qa_ms, qw_ms, g_ms = reduce_max([ms] + k_ms, dev)
 
     # end to end through the C ABI from pinned host buffers: H2D of A and W, the three calls,
     # D2H of C, every step
-    e2e = None
-    if rank == 0 or world > 1:
-        a_h = a.cpu().pin_memory()
-        w_h = w.cpu().pin_memory()
-        c_h = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
-        e2e_steps = max(3, min(10, args.steps))
-        for i in range(e2e_steps + 1):
-            if i == 1:
-                torch.cuda.synchronize(dev)
-                s0 = torch.cuda.Event(enable_timing=True)
-                s0.record(stream)
-            a.copy_(a_h, non_blocking=True)
-            w.copy_(w_h, non_blocking=True)
-            step()
-            c_h.copy_(c, non_blocking=True)
-        s1 = torch.cuda.Event(enable_timing=True)
-        s1.record(stream)
-        torch.cuda.synchronize(dev)
-        e2e_ms = s0.elapsed_time(s1) / e2e_steps
-        e2e = {"value": round(gemm_flops(M, N, K) * world / (e2e_ms * 1e-3) / 1e12, 2),
-               "unit": "TFLOP/s",
-               "h2d_bytes_per_step": a.numel() * 2 + w.numel() * 2,
-               "d2h_bytes_per_step": c.numel() * 2,
-               "ms_per_step": round(e2e_ms, 4)}
+    a_h = a.cpu().pin_memory()
+    w_h = w.cpu().pin_memory()
+    c_h = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
+    e2e_steps = max(3, min(10, args.steps))
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(e2e_steps + 1):
+        if i == 1:                          # the first pass is a warm-up
+            torch.cuda.synchronize(dev)
+            s0.record(stream)
+        a.copy_(a_h, non_blocking=True)
+        w.copy_(w_h, non_blocking=True)
+        step()
+        c_h.copy_(c, non_blocking=True)
+    s1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = reduce_max([s0.elapsed_time(s1) / e2e_steps], dev)[0]
+    e2e = {"value": round(gemm_flops(M, N, K) * world / (e2e_ms * 1e-3) / 1e12, 2),
+           "unit": "TFLOP/s",
+           "h2d_bytes_per_step": a.numel() * 2 + w.numel() * 2,
+           "d2h_bytes_per_step": c.numel() * 2,
+           "ms_per_step": round(e2e_ms, 4)}
 
     peaks, peak_src = load_peaks()
     fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
@@ -288,9 +291,108 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": 3 * args.steps,
         "clocks": clk,
     }
+    if not args.no_extras:
+        del a, w, aq, a_s, wq, w_s, c, a_h, w_h, c_h
+        torch.cuda.empty_cache()
+        line["workloads"] = run_extras(F, dev, peaks, fp8_peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget_s)
     return line
+
+
+# --------------------------------------------------------------------------------------
+# The other workloads, each kernel timed alone (L2 flushed between iterations)
+# --------------------------------------------------------------------------------------
+
+def _timed(fn, dev, iters=10, warm=3):
+    """Mean device time (ms) of fn(), with a 256 MB write flushing L2 before every run."""
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    times = []
+    for i in range(warm + iters):
+        flush.fill_(i & 0xFF)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        if i >= warm:
+            times.append((e0, e1))
+    torch.cuda.synchronize(dev)
+    return statistics.mean(a.elapsed_time(b) for a, b in times)
+
+
+def run_extras(F, dev, peaks, fp8_peak):
+    out = {"timing": "each kernel alone, L2 flushed (256 MB write) before every iteration, "
+                     "mean of 10 after 3 warm-up"}
+    hbm = peaks["hbm_gbs"]
+    # quantizer bandwidth sweep
+    sweep = {}
+    for M in WL.SWEEP_ACT_M:
+        x = WL.sweep_activations(M, dev)
+        q = torch.empty(M, WL.SWEEP_K, dtype=torch.uint8, device=dev)
+        s = torch.empty(WL.SWEEP_K // 128, M, dtype=torch.float32, device=dev)
+        ms = _timed(lambda: F.fp8_quant_act_1x128(x, q, s), dev)
+        gbs = M * WL.SWEEP_K * ACT_BYTES_PER_ELEM / (ms * 1e-3) / 1e9
+        sweep[f"act_{M}x{WL.SWEEP_K}"] = {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
+                                          "frac_hbm": round(gbs / hbm, 4)}
+        del x, q, s
+    wt = WL.sweep_weight(dev)
+    q = torch.empty_like(wt, dtype=torch.uint8)
+    s = torch.empty(WL.SWEEP_W_N // 128, WL.SWEEP_W_K // 128, dtype=torch.float32, device=dev)
+    ms = _timed(lambda: F.fp8_quant_weight_128x128(wt, q, s), dev)
+    gbs = wt.numel() * W_BYTES_PER_ELEM / (ms * 1e-3) / 1e9
+    sweep[f"weight_{WL.SWEEP_W_N}x{WL.SWEEP_W_K}"] = {"us": round(ms * 1e3, 2),
+                                                      "GB/s": round(gbs, 1),
+                                                      "frac_hbm": round(gbs / hbm, 4)}
+    del wt, q, s
+    out["quantizer_sweep"] = sweep
+    # MLA projections
+    mla = {}
+    for shape in WL.MLA:
+        a, w = WL.gemm_inputs(shape, dev)
+        aq, a_s = F.fp8_quant_act_1x128(a)
+        wq, w_s = F.fp8_quant_weight_128x128(w)
+        c = torch.empty(a.shape[0], w.shape[0], dtype=torch.bfloat16, device=dev)
+        ms = _timed(lambda: F.fp8_blockscaled_gemm(aq, a_s, wq, w_s, out=c), dev)
+        tf = gemm_flops(a.shape[0], w.shape[0], a.shape[1]) / (ms * 1e-3) / 1e12
+        mla[shape.name] = {"us": round(ms * 1e3, 1), "TFLOP/s": round(tf, 1),
+                           "frac_fp8_peak": round(tf / fp8_peak, 4), "N_run": w.shape[0]}
+        del a, w, aq, a_s, wq, w_s, c
+    out["mla_gemm"] = mla
+    # MoE grouped GEMMs
+    moe = {}
+    shape = WL.MOE
+    off, token_of_row = WL.moe_routing(shape)
+    R = int(off[-1])
+    offs = torch.from_numpy(off).to(dev)
+    for which in ("gate_up", "down"):
+        if which == "gate_up":
+            N, K = shape.n_gate_up, shape.hidden
+            a = WL.moe_tokens(shape, dev)[torch.from_numpy(token_of_row).to(dev)]
+        else:
+            N, K = shape.hidden, shape.k_down
+            a = WL.moe_down_input(shape, R, dev)
+        wts = WL.moe_expert_weights(shape, N, K, which, dev)
+        aq, a_s = F.fp8_quant_act_1x128(a)
+        wq, w_s = F.fp8_quant_weight_128x128(wts.view(-1, K))
+        del wts
+        wq = wq.view(shape.experts, N, K)
+        w_s = w_s.view(shape.experts, N // 128, K // 128)
+        c = torch.empty(R, N, dtype=torch.bfloat16, device=dev)
+        ms = _timed(lambda: F.fp8_blockscaled_grouped_gemm(aq, a_s, wq, w_s, offs, out=c), dev)
+        tf = gemm_flops(R, N, K) / (ms * 1e-3) / 1e12
+        algo_bytes = wq.numel() + aq.numel() + c.numel() * 2 + a_s.numel() * 4 + w_s.numel() * 4
+        gbs = algo_bytes / (ms * 1e-3) / 1e9
+        moe[which] = {"us": round(ms * 1e3, 1), "TFLOP/s": round(tf, 1),
+                      "frac_fp8_peak": round(tf / fp8_peak, 4), "GB/s": round(gbs, 1),
+                      "frac_hbm": round(gbs / hbm, 4), "R": R, "N": N, "K": K,
+                      "experts": shape.experts}
+        del a, aq, a_s, wq, w_s, c
+        torch.cuda.empty_cache()
+    out["moe_grouped_gemm"] = moe
+    if F.fp8bs_last_error() != F.FP8BS_OK:
+        raise RuntimeError("a kernel reported a pipeline timeout in the extra workloads")
+    return out
 
 
 # --------------------------------------------------------------------------------------
@@ -415,6 +517,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle timing on the host cores")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the quantizer sweep, MLA and MoE workloads")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

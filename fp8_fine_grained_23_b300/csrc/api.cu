@@ -159,8 +159,9 @@ int fp8_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_
     if (st != FP8BS_OK || M == 0) return st;
     DeviceInfo* d = nullptr;
     if ((st = current_device(&d)) != FP8BS_OK) return st;
-    return cuda_status(launch_quant_act(x, M, K, ldx, q, ldq, scales, d->num_sms,
-                                        reinterpret_cast<cudaStream_t>(stream)));
+    if ((st = ensure_error_word(d)) != FP8BS_OK) return st;
+    return cuda_status(launch_quant_act(x, M, K, ldx, q, ldq, scales, d->num_sms, d->err,
+                                        wait_budget(), reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int fp8_quant_weight_128x128(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
@@ -186,9 +187,10 @@ int fp8_blockscaled_gemm(const uint8_t* a_q, const float* a_s, const uint8_t* w_
     if ((st = ensure_error_word(d)) != FP8BS_OK) return st;
     if ((st = ensure_encoder()) != FP8BS_OK) return st;
 
+    const int cluster = gemm_cluster_size(false);
     CUtensorMap ma, mb;
     if ((st = make_code_map(&ma, a_q, K, M, K, GEMM_BM)) != FP8BS_OK) return st;
-    if ((st = make_code_map(&mb, w_q, K, N, K, GEMM_BN)) != FP8BS_OK) return st;
+    if ((st = make_code_map(&mb, w_q, K, N, K, GEMM_BN / cluster)) != FP8BS_OK) return st;
 
     GemmArgs args{};
     args.a_s = a_s;
@@ -201,15 +203,14 @@ int fp8_blockscaled_gemm(const uint8_t* a_q, const float* a_s, const uint8_t* w_
     args.NB = static_cast<int>((N + 127) / 128);
     args.NT = static_cast<int>((N + GEMM_BN - 1) / GEMM_BN);
     args.MT = static_cast<int>((M + GEMM_BM - 1) / GEMM_BM);
-    const int64_t tiles = static_cast<int64_t>(args.MT) * args.NT;
-    if (tiles > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
-    args.num_tiles = static_cast<int>(tiles);
+    const int64_t items = static_cast<int64_t>((args.MT + cluster - 1) / cluster) * args.NT;
+    if (items > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
+    args.num_tiles = static_cast<int>(items);
     args.offsets = nullptr;
     args.G = 1;
     args.err = d->err;
     args.budget = wait_budget();
-    const int grid = static_cast<int>(tiles < d->num_sms ? tiles : d->num_sms);
-    return cuda_status(launch_gemm(ma, mb, args, false, out_dtype == FP8BS_OUT_F32, grid,
+    return cuda_status(launch_gemm(ma, mb, args, false, out_dtype == FP8BS_OUT_F32, d->num_sms,
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -253,8 +254,8 @@ int fp8_blockscaled_grouped_gemm(const uint8_t* a_q, const float* a_s, const uin
     // device from the offsets, and CTAs without a tile exit at once.
     const int64_t bound = ((R + GEMM_BM - 1) / GEMM_BM + G) * args.NT;
     if (bound > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
-    const int grid = static_cast<int>(bound < d->num_sms ? bound : d->num_sms);
-    return cuda_status(launch_gemm(ma, mb, args, true, out_dtype == FP8BS_OUT_F32, grid,
+    const int max_ctas = static_cast<int>(bound < d->num_sms ? bound : d->num_sms);
+    return cuda_status(launch_gemm(ma, mb, args, true, out_dtype == FP8BS_OUT_F32, max_ctas,
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -19,10 +19,17 @@
 //   warps 2-3  idle after set-up (warp 0 also builds the group table of the grouped variant);
 //   warps 4-11 epilogue: warp w reads TMEM lanes 32*(w%4).. (its rows) and columns
 //              128*((w-4)/4).. (one weight block), promotes each K block's partial into 128
-//              FP32 registers per thread, and writes the finished tile (BF16 or FP32).
+//              FP32 registers per thread (packed pairs, fma.rn.f32x2), and writes the
+//              finished tile (BF16 or FP32).
+// Dense GEMMs run as clusters of two CTAs on adjacent m-tiles of the same n-tile: each CTA loads
+// its own A tile and one half (128 rows) of the shared W tile, multicast into both CTAs' shared
+// memory, which cuts the L2-to-SM traffic per K block from 48 KB to 32 KB per CTA. A stage is
+// free again only when both CTAs' MMAs have read it, so each MMA commit is multicast to the
+// empty barriers of both CTAs (count 2). A cluster barrier after set-up and before exit keeps
+// every remote arrival and multicast write inside both CTAs' lifetimes.
 // Registers: the launch gives 168 per thread (65536 / 384, rounded to 8). Warpgroup 0 drops to
 // 56 and the two epilogue warpgroups rise to 224 (128*56 + 256*224 = 384*168), which holds the
-// 128 accumulators and 64 staging registers of a thread without spilling.
+// 128 accumulators and 32 staging registers of an epilogue thread.
 // Every mbarrier wait is bounded (clock budget); on expiry the CTA records an error code in the
 // device error word, stops issuing work, waits for its in-flight copies and MMAs, frees TMEM and
 // returns.
@@ -38,7 +45,6 @@ namespace {
 constexpr int BM = GEMM_BM;
 constexpr int BN = GEMM_BN;
 constexpr int BK = GEMM_BK;
-constexpr int STAGES = 4;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int PRODUCER_WARP = 0;
 constexpr int MMA_WARP = 1;
@@ -53,13 +59,23 @@ constexpr int TMEM_COLS = 2 * BN;          // two FP32 accumulators of 128 lanes
 constexpr int A_BYTES = BM * BK;           // E4M3: one byte per element
 constexpr int B_BYTES = BN * BK;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int A_OFF = 0;
-constexpr int B_OFF = STAGES * A_BYTES;
-constexpr int BAR_OFF = STAGES * STAGE_BYTES;
-constexpr int NUM_BARS = 2 * STAGES + 5;   // full[S], empty[S], tfull[2], tempty[2], drain
-constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
-constexpr int GROUP_OFF = MISC_OFF + 16;
+constexpr int STG_WARP_BYTES = 32 * 128;   // output staging per epilogue warp: 32 rows x 128 B
+constexpr int STG_BYTES = NUM_EPI_WARPS * STG_WARP_BYTES;
 constexpr int ALIGN_PAD = 1024;            // 128-byte-swizzled tiles need 1024-byte alignment
+
+// Shared-memory layout. The dense kernel keeps four 48 KB stages; the grouped kernel, which is
+// bound by streaming expert weights from HBM, keeps three and leaves room for its group table.
+template <bool GROUPED>
+struct Layout {
+    static constexpr int STAGES = GROUPED ? 3 : 4;
+    static constexpr int A_OFF = 0;
+    static constexpr int B_OFF = STAGES * A_BYTES;
+    static constexpr int STG_OFF = STAGES * STAGE_BYTES;
+    static constexpr int BAR_OFF = STG_OFF + STG_BYTES;
+    static constexpr int NUM_BARS = 2 * STAGES + 5;   // full[S], empty[S], tfull[2], tempty[2], drain
+    static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
+    static constexpr int GROUP_OFF = MISC_OFF + 16;
+};
 
 static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "tiles must keep 1024-B alignment");
 
@@ -71,20 +87,25 @@ struct TileInfo {
     int g;             // group (0 for dense)
 };
 
-__device__ __forceinline__ void raise_error(int* err, volatile int* abort_flag, int code)
+__device__ __forceinline__ void raise_error(int* err, uint32_t abort_addr, int code)
 {
-    *abort_flag = 1;
+    st_shared_volatile_u32(abort_addr, 1u);
     atomicCAS(err, 0, code);
 }
 
-template <bool GROUPED>
+// Work item t of a CTA whose rank in its cluster is `crank`. Dense: t numbers groups of
+// CLUSTER adjacent m-tiles (one per CTA of the cluster) on one n-tile, m fastest; an m-tile past
+// the last row reads zeros and stores nothing. Grouped (CLUSTER == 1): t numbers
+// (group, n-tile, m-tile) with m fastest.
+template <bool GROUPED, int CLUSTER>
 __device__ __forceinline__ TileInfo decode_tile(int t, const GemmArgs& p, const int* s_tstart,
-                                                const int* s_off)
+                                                const int* s_off, int crank)
 {
     TileInfo ti;
     if constexpr (!GROUPED) {
-        const int mt = t % p.MT;
-        const int nt = t / p.MT;
+        const int mgroups = (p.MT + CLUSTER - 1) / CLUSTER;
+        const int mt = (t % mgroups) * CLUSTER + crank;
+        const int nt = t / mgroups;
         ti.row0 = static_cast<int64_t>(mt) * BM;
         ti.row_end = p.rows;
         ti.n0 = nt * BN;
@@ -132,6 +153,23 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return r;
 }
 
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4& v)
+{
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void st_v4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
 {
     asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c),
@@ -139,44 +177,51 @@ __device__ __forceinline__ void st_v4(void* p, uint32_t a, uint32_t b, uint32_t 
                  : "memory");
 }
 
-template <bool GROUPED, bool OUT_F32>
+template <bool GROUPED, bool OUT_F32, int CLUSTER>
 __global__ void __launch_bounds__(THREADS, 1)
 fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                             const __grid_constant__ CUtensorMap map_b, const GemmArgs p)
 {
+    using L = Layout<GROUPED>;
+    constexpr int STAGES = L::STAGES;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + (ALIGN_PAD - 1)) & ~static_cast<uint32_t>(ALIGN_PAD - 1);
     uint8_t* smem = smem_raw + (base - raw);
 
-    const uint32_t sA = base + A_OFF;
-    const uint32_t sB = base + B_OFF;
-    const uint32_t bar0 = base + BAR_OFF;
+    const uint32_t sA = base + L::A_OFF;
+    const uint32_t sB = base + L::B_OFF;
+    const uint32_t bar0 = base + L::BAR_OFF;
     const uint32_t full0 = bar0;
     const uint32_t empty0 = bar0 + 8 * STAGES;
     const uint32_t tfull0 = bar0 + 16 * STAGES;
     const uint32_t tempty0 = tfull0 + 16;
     const uint32_t drain_bar = tempty0 + 16;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + MISC_OFF);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + MISC_OFF + 4);
-    int* s_tstart = reinterpret_cast<int*>(smem + GROUP_OFF);   // grouped: [G+1]
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
+    const uint32_t abort_addr = base + L::MISC_OFF + 4;   // shared word: a role gave up
+    int* s_tstart = reinterpret_cast<int*>(smem + L::GROUP_OFF);   // grouped: [G+1]
     int* s_off = s_tstart + (p.G + 1);                            // grouped: [G+1]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const long long budget = p.budget;
+    const int crank = CLUSTER > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+    const int cluster_id = blockIdx.x / CLUSTER;
+    const int num_clusters = gridDim.x / CLUSTER;
+    constexpr uint16_t CLUSTER_MASK = static_cast<uint16_t>((1u << CLUSTER) - 1u);
+    constexpr int B_PART = B_BYTES / CLUSTER;     // W rows loaded (and multicast) by each CTA
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; s++) {
             mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, CLUSTER);   // one commit from every CTA of the cluster
         }
         for (int b = 0; b < 2; b++) {
             mbar_init(tfull0 + 8 * b, 1);
             mbar_init(tempty0 + 8 * b, NUM_EPI_WARPS);
         }
         mbar_init(drain_bar, 1);
-        *abort_flag = 0;
+        st_shared_volatile_u32(abort_addr, 0u);
         fence_mbar_init();
     }
     if (warp == PRODUCER_WARP && lane == 0) {
@@ -213,6 +258,7 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (CLUSTER > 1) cluster_sync();   // peers' barriers exist before any multicast
     tc_fence_after();
 
     const uint32_t tmem_base = *tmem_holder;
@@ -227,21 +273,28 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
             if (lane == 0) {
                 uint32_t it = 0;
                 bool ok = true;
-                for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-                    const TileInfo ti = decode_tile<GROUPED>(t, p, s_tstart, s_off);
+                for (int t = cluster_id; ok && t < num_tiles; t += num_clusters) {
+                    const TileInfo ti = decode_tile<GROUPED, CLUSTER>(t, p, s_tstart, s_off, crank);
                     for (int kb = 0; kb < KB; kb++, it++) {
                         const uint32_t s = it % STAGES;
                         const uint32_t ph = (it / STAGES) & 1u;
-                        if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, abort_flag, budget)) {
-                            raise_error(p.err, abort_flag, DEV_TIMEOUT_PRODUCER);
+                        if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, abort_addr, budget)) {
+                            raise_error(p.err, abort_addr, DEV_TIMEOUT_PRODUCER);
                             ok = false;
                             break;
                         }
                         mbar_arrive_expect_tx(full0 + 8 * s, STAGE_BYTES);
                         tma_load_2d(sA + s * A_BYTES, &map_a, full0 + 8 * s, kb * BK,
                                     static_cast<int32_t>(ti.row0));
-                        tma_load_2d(sB + s * B_BYTES, &map_b, full0 + 8 * s, kb * BK,
-                                    static_cast<int32_t>(ti.wrow0));
+                        if constexpr (CLUSTER == 1) {
+                            tma_load_2d(sB + s * B_BYTES, &map_b, full0 + 8 * s, kb * BK,
+                                        static_cast<int32_t>(ti.wrow0));
+                        } else {
+                            tma_load_2d_multicast(sB + s * B_BYTES + crank * B_PART, &map_b,
+                                                  full0 + 8 * s, kb * BK,
+                                                  static_cast<int32_t>(ti.wrow0 + crank * (BN / CLUSTER)),
+                                                  CLUSTER_MASK);
+                        }
                     }
                 }
                 if (!ok) {
@@ -249,7 +302,7 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     // issued into every stage before the CTA may exit.
                     const uint32_t first = it > STAGES ? it - STAGES : 0;
                     for (uint32_t i = first; i < it; i++)
-                        if (!mbar_wait(full0 + 8 * (i % STAGES), (i / STAGES) & 1u, nullptr, budget))
+                        if (!mbar_wait(full0 + 8 * (i % STAGES), (i / STAGES) & 1u, 0u, budget))
                             atomicCAS(p.err, 0, DEV_TIMEOUT_DRAIN);
                 }
             }
@@ -259,19 +312,19 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                 constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN);
                 uint32_t it = 0, j = 0;
                 bool ok = true, issued = false;
-                for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+                for (int t = cluster_id; ok && t < num_tiles; t += num_clusters) {
                     for (int kb = 0; kb < KB; kb++, it++, j++) {
                         const uint32_t b = j & 1u;
                         const uint32_t pb = (j >> 1) & 1u;
-                        if (!mbar_wait(tempty0 + 8 * b, pb ^ 1u, abort_flag, budget)) {
-                            raise_error(p.err, abort_flag, DEV_TIMEOUT_MMA_TMEM);
+                        if (!mbar_wait(tempty0 + 8 * b, pb ^ 1u, abort_addr, budget)) {
+                            raise_error(p.err, abort_addr, DEV_TIMEOUT_MMA_TMEM);
                             ok = false;
                             break;
                         }
                         const uint32_t s = it % STAGES;
                         const uint32_t ph = (it / STAGES) & 1u;
-                        if (!mbar_wait(full0 + 8 * s, ph, abort_flag, budget)) {
-                            raise_error(p.err, abort_flag, DEV_TIMEOUT_MMA_FULL);
+                        if (!mbar_wait(full0 + 8 * s, ph, abort_addr, budget)) {
+                            raise_error(p.err, abort_addr, DEV_TIMEOUT_MMA_FULL);
                             ok = false;
                             break;
                         }
@@ -282,7 +335,8 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     #pragma unroll
                         for (int k = 0; k < BK / 32; k++)   // +32 bytes of K = +2 in the address field
                             mma_e4m3(d_tmem, da + 2 * k, db + 2 * k, IDESC, k > 0 ? 1u : 0u);
-                        mma_commit(empty0 + 8 * s);
+                        if constexpr (CLUSTER == 1) mma_commit(empty0 + 8 * s);
+                        else mma_commit_multicast(empty0 + 8 * s, CLUSTER_MASK);
                         mma_commit(tfull0 + 8 * b);
                         issued = true;
                     }
@@ -290,7 +344,7 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                 if (issued) {
                     // Every MMA must have finished before TMEM is released.
                     mma_commit(drain_bar);
-                    if (!mbar_wait(drain_bar, 0, nullptr, budget)) atomicCAS(p.err, 0, DEV_TIMEOUT_DRAIN);
+                    if (!mbar_wait(drain_bar, 0, 0u, budget)) atomicCAS(p.err, 0, DEV_TIMEOUT_DRAIN);
                 }
             }
             __syncwarp();
@@ -303,10 +357,10 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
         const int r = quad * 32 + lane;         // row within the tile
         const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
         uint32_t j = 0;
-        float acc[128];
+        uint64_t acc[64];   // 128 FP32 accumulators as packed pairs (columns 2i, 2i + 1)
 
-        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-            const TileInfo ti = decode_tile<GROUPED>(t, p, s_tstart, s_off);
+        for (int t = cluster_id; t < num_tiles; t += num_clusters) {
+            const TileInfo ti = decode_tile<GROUPED, CLUSTER>(t, p, s_tstart, s_off, crank);
             const int64_t row = ti.row0 + r;
             const bool row_ok = row >= 0 && row < ti.row_end;
             const int ncol0 = ti.n0 + half * 128;
@@ -314,42 +368,49 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
             const float* sa_ptr = p.a_s + (row_ok ? row : 0);
             const float* sw_ptr =
                 p.w_s + (static_cast<int64_t>(ti.g) * p.NB + (blk_ok ? ncol0 / 128 : 0)) * KB;
-            float sa_next = row_ok ? __ldg(sa_ptr) : 0.0f;
-            float sw_next = blk_ok ? __ldg(sw_ptr) : 0.0f;
+            // Scales are prefetched two K blocks ahead so that their load latency stays hidden.
+            float sa_c = row_ok ? __ldg(sa_ptr) : 0.0f;
+            float sw_c = blk_ok ? __ldg(sw_ptr) : 0.0f;
+            float sa_n = (row_ok && KB > 1) ? __ldg(sa_ptr + p.rows) : 0.0f;
+            float sw_n = (blk_ok && KB > 1) ? __ldg(sw_ptr + 1) : 0.0f;
 
 #pragma unroll
-            for (int i = 0; i < 128; i++) acc[i] = 0.0f;
+            for (int i = 0; i < 64; i++) acc[i] = 0ull;
 
             bool ok = true;
             for (int kb = 0; kb < KB; kb++, j++) {
-                const float sc = __fmul_rn(sa_next, sw_next);
-                if (kb + 1 < KB) {
-                    sa_next = row_ok ? __ldg(sa_ptr + static_cast<int64_t>(kb + 1) * p.rows) : 0.0f;
-                    sw_next = blk_ok ? __ldg(sw_ptr + kb + 1) : 0.0f;
+                const float sc = __fmul_rn(sa_c, sw_c);
+                sa_c = sa_n;
+                sw_c = sw_n;
+                if (kb + 2 < KB) {
+                    sa_n = row_ok ? __ldg(sa_ptr + static_cast<int64_t>(kb + 2) * p.rows) : 0.0f;
+                    sw_n = blk_ok ? __ldg(sw_ptr + kb + 2) : 0.0f;
                 }
                 const uint32_t b = j & 1u;
                 const uint32_t pb = (j >> 1) & 1u;
-                const bool got = mbar_wait(tfull0 + 8 * b, pb, abort_flag, budget);
+                const bool got = mbar_wait(tfull0 + 8 * b, pb, abort_addr, budget);
                 if (!__all_sync(0xffffffffu, got)) {
-                    if (lane == 0) raise_error(p.err, abort_flag, DEV_TIMEOUT_EPILOGUE);
+                    if (lane == 0) raise_error(p.err, abort_addr, DEV_TIMEOUT_EPILOGUE);
                     ok = false;
                     break;
                 }
                 tc_fence_after();
+                // Eight 16-column chunks; the TMEM load of chunk c+1 is in flight while chunk c
+                // is promoted (two register buffers of 8 packed pairs).
                 const uint32_t taddr = tmem_base + t_lane + b * BN + half * 128;
+                const uint64_t sc2 = f32x2_splat(sc);
+                uint64_t v0[8], v1[8];
+                tmem_ld_16cols(taddr, v0);
 #pragma unroll
-                for (int c = 0; c < 4; c += 2) {
-                    uint32_t v0[32], v1[32];
-                    tmem_ld_32cols(taddr + c * 32, v0);
-                    tmem_ld_32cols(taddr + (c + 1) * 32, v1);
-                    tmem_wait_ld();
+                for (int c = 0; c < 8; c += 2) {
+                    tmem_wait_ld(v0);
+                    tmem_ld_16cols(taddr + (c + 1) * 16, v1);
 #pragma unroll
-                    for (int i = 0; i < 32; i++)
-                        acc[c * 32 + i] = fmaf(__uint_as_float(v0[i]), sc, acc[c * 32 + i]);
+                    for (int i = 0; i < 8; i++) ffma2(acc[c * 8 + i], v0[i], sc2);
+                    tmem_wait_ld(v1);
+                    if (c + 2 < 8) tmem_ld_16cols(taddr + (c + 2) * 16, v0);
 #pragma unroll
-                    for (int i = 0; i < 32; i++)
-                        acc[(c + 1) * 32 + i] =
-                            fmaf(__uint_as_float(v1[i]), sc, acc[(c + 1) * 32 + i]);
+                    for (int i = 0; i < 8; i++) ffma2(acc[(c + 1) * 8 + i], v1[i], sc2);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -357,24 +418,46 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
             }
             if (!ok) break;
 
-            if (row_ok) {
-                if constexpr (OUT_F32) {
-                    float* crow = static_cast<float*>(p.c) + row * p.ldc + ncol0;
+            // Store: stage this warp's 32 rows x 128 B at a time in shared memory (16-byte chunk j
+            // of row r at chunk j ^ (r % 8): conflict-free both ways), then write 4 whole rows of
+            // 128 B per warp instruction instead of 32 scattered 16-byte pieces.
+            {
+                constexpr int ELEM = OUT_F32 ? 4 : 2;
+                constexpr int GCOLS = 128 / ELEM;            // columns per 128-byte staged row
+                const TileInfo ts = decode_tile<GROUPED, CLUSTER>(t, p, s_tstart, s_off, crank);
+                const uint32_t stg = base + L::STG_OFF + (warp - EPI_WARP0) * STG_WARP_BYTES;
+                const int64_t wrow0 = ts.row0 + quad * 32;   // first row of this warp
 #pragma unroll
-                    for (int i = 0; i < 32; i++)
-                        if (ncol0 + 4 * i < p.N)
-                            st_v4(crow + 4 * i, __float_as_uint(acc[4 * i]),
-                                  __float_as_uint(acc[4 * i + 1]), __float_as_uint(acc[4 * i + 2]),
-                                  __float_as_uint(acc[4 * i + 3]));
-                } else {
-                    uint16_t* crow = static_cast<uint16_t*>(p.c) + row * p.ldc + ncol0;
+                for (int g = 0; g < 128 / GCOLS; g++) {
 #pragma unroll
-                    for (int i = 0; i < 16; i++)
-                        if (ncol0 + 8 * i < p.N)
-                            st_v4(crow + 8 * i, pack_bf16x2(acc[8 * i], acc[8 * i + 1]),
-                                  pack_bf16x2(acc[8 * i + 2], acc[8 * i + 3]),
-                                  pack_bf16x2(acc[8 * i + 4], acc[8 * i + 5]),
-                                  pack_bf16x2(acc[8 * i + 6], acc[8 * i + 7]));
+                    for (int jc = 0; jc < 8; jc++) {
+                        uint4 v;
+                        if constexpr (OUT_F32) {
+                            const uint64_t p0 = acc[g * 16 + jc * 2], p1 = acc[g * 16 + jc * 2 + 1];
+                            v = make_uint4(static_cast<uint32_t>(p0), static_cast<uint32_t>(p0 >> 32),
+                                           static_cast<uint32_t>(p1), static_cast<uint32_t>(p1 >> 32));
+                        } else {
+                            const int q = g * 32 + jc * 4;
+                            v = make_uint4(pack_bf16x2(f32x2_lo(acc[q]), f32x2_hi(acc[q])),
+                                           pack_bf16x2(f32x2_lo(acc[q + 1]), f32x2_hi(acc[q + 1])),
+                                           pack_bf16x2(f32x2_lo(acc[q + 2]), f32x2_hi(acc[q + 2])),
+                                           pack_bf16x2(f32x2_lo(acc[q + 3]), f32x2_hi(acc[q + 3])));
+                        }
+                        st_shared_v4(stg + lane * 128 + ((jc ^ (lane & 7)) * 16), v);
+                    }
+                    __syncwarp();
+                    const int ch = lane & 7;
+                    const int gcol = ncol0 + g * GCOLS + ch * (16 / ELEM);
+#pragma unroll
+                    for (int i = 0; i < 8; i++) {
+                        const int rr = i * 4 + (lane >> 3);
+                        const uint4 v = ld_shared_v4(stg + rr * 128 + ((ch ^ (rr & 7)) * 16));
+                        const int64_t grow = wrow0 + rr;
+                        if (grow >= 0 && grow < ts.row_end && gcol < p.N)
+                            st_v4(static_cast<uint8_t*>(p.c) + (grow * p.ldc + gcol) * ELEM, v.x, v.y,
+                                  v.z, v.w);
+                    }
+                    __syncwarp();
                 }
             }
         }
@@ -387,18 +470,49 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
         __syncwarp();
         tmem_dealloc(tmem_base, TMEM_COLS);
     }
+    if constexpr (CLUSTER > 1) cluster_sync();   // no peer still targets this CTA's memory
 }
 
-template <bool GROUPED, bool OUT_F32>
+template <bool GROUPED, bool OUT_F32, int CLUSTER>
 cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& args,
-                       int grid, cudaStream_t stream)
+                       int max_ctas, cudaStream_t stream)
 {
-    auto kern = fp8_blockscaled_gemm_kernel<GROUPED, OUT_F32>;
+    auto kern = fp8_blockscaled_gemm_kernel<GROUPED, OUT_F32, CLUSTER>;
     const size_t smem = gemm_smem_bytes(GROUPED, args.G);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    kern<<<grid, THREADS, smem, stream>>>(ma, mb, args);
+    if (CLUSTER > 1) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CLUSTER;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // Persistent grid: as many clusters as fit at once (one CTA per SM), at most one per item.
+    int clusters = max_ctas / CLUSTER;
+    if (CLUSTER > 1) {
+        cfg.gridDim = dim3(static_cast<unsigned>(clusters * CLUSTER));
+        int active = 0;
+        if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) != cudaSuccess) {
+            cudaGetLastError();   // not fatal: keep one cluster per SM pair
+            active = 0;
+        }
+        if (active > 0 && active < clusters) clusters = active;
+    }
+    if (!GROUPED && args.num_tiles < clusters) clusters = args.num_tiles;
+    if (clusters < 1) clusters = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * CLUSTER));
+    e = cudaLaunchKernelEx(&cfg, kern, ma, mb, args);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
@@ -406,19 +520,22 @@ cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const GemmA
 
 size_t gemm_smem_bytes(bool grouped, int G)
 {
-    size_t bytes = static_cast<size_t>(GROUP_OFF) + ALIGN_PAD;
-    if (grouped) bytes += 2 * static_cast<size_t>(G + 1) * sizeof(int);
-    return bytes;
+    if (!grouped) return static_cast<size_t>(Layout<false>::GROUP_OFF) + ALIGN_PAD;
+    return static_cast<size_t>(Layout<true>::GROUP_OFF) + ALIGN_PAD +
+           2 * static_cast<size_t>(G + 1) * sizeof(int);
 }
 
+int gemm_cluster_size(bool grouped) { return grouped ? 1 : GEMM_DENSE_CLUSTER; }
+
 cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args,
-                        bool grouped, bool out_f32, int grid, cudaStream_t stream)
+                        bool grouped, bool out_f32, int max_ctas, cudaStream_t stream)
 {
     if (grouped)
-        return out_f32 ? launch_one<true, true>(map_a, map_b, args, grid, stream)
-                       : launch_one<true, false>(map_a, map_b, args, grid, stream);
-    return out_f32 ? launch_one<false, true>(map_a, map_b, args, grid, stream)
-                   : launch_one<false, false>(map_a, map_b, args, grid, stream);
+        return out_f32 ? launch_one<true, true, 1>(map_a, map_b, args, max_ctas, stream)
+                       : launch_one<true, false, 1>(map_a, map_b, args, max_ctas, stream);
+    return out_f32
+               ? launch_one<false, true, GEMM_DENSE_CLUSTER>(map_a, map_b, args, max_ctas, stream)
+               : launch_one<false, false, GEMM_DENSE_CLUSTER>(map_a, map_b, args, max_ctas, stream);
 }
 
 }  // namespace fp8bs

@@ -15,6 +15,7 @@ constexpr int GEMM_BM = 128;
 constexpr int GEMM_BN = 256;
 constexpr int GEMM_BK = 128;
 constexpr int GEMM_MAX_GROUPS = 1024;
+constexpr int GEMM_DENSE_CLUSTER = 2;   // dense GEMM: CTA pairs sharing (multicasting) W tiles
 
 // Device error word codes (the first error of a launch wins).
 enum DeviceError : int {
@@ -37,7 +38,7 @@ struct GemmArgs {
     int NB;                   // ceil(N / 128)
     int NT;                   // ceil(N / GEMM_BN)
     int MT;                   // dense: ceil(M / 128)
-    int num_tiles;            // dense: MT * NT (grouped: computed on the device)
+    int num_tiles;            // dense: work items = ceil(MT / cluster) * NT (grouped: on device)
     const int32_t* offsets;   // grouped: [G+1] on the device
     int G;
     int* err;                 // device error word
@@ -45,11 +46,14 @@ struct GemmArgs {
 };
 
 cudaError_t launch_quant_act(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
-                             int64_t ldq, float* scales, int num_sms, cudaStream_t stream);
+                             int64_t ldq, float* scales, int num_sms, int* err, long long budget,
+                             cudaStream_t stream);
 cudaError_t launch_quant_weight(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
                                 int64_t ldq, float* scales, cudaStream_t stream);
+// max_ctas: the persistent grid's upper bound (the SM count); the launcher sizes the grid.
 cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args,
-                        bool grouped, bool out_f32, int grid, cudaStream_t stream);
+                        bool grouped, bool out_f32, int max_ctas, cudaStream_t stream);
+int gemm_cluster_size(bool grouped);
 size_t gemm_smem_bytes(bool grouped, int G);
 
 }  // namespace fp8bs

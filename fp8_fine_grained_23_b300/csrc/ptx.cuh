@@ -50,16 +50,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+__device__ __forceinline__ uint32_t ld_shared_volatile_u32(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_shared_volatile_u32(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 // Waits until the phase with the given parity has completed. Gives up (returns false) when
-// `budget` SM clock cycles have passed or when another role of the CTA has raised `*abort`.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort,
+// `budget` SM clock cycles have passed or when another role of the CTA has set the shared word
+// at `abort_addr` (0: no abort word).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t abort_addr,
                                           long long budget)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (abort != nullptr && *abort) return false;
+        if (abort_addr != 0 && ld_shared_volatile_u32(abort_addr) != 0) return false;
         if (clock64() - t0 > budget) return false;
     }
 }
@@ -81,6 +94,56 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(map), "r"(x), "r"(y), "r"(bar)
         : "memory");
+}
+
+// Same load, written to the same shared-memory offset of every CTA in `cta_mask` (cluster
+// multicast); each destination CTA's mbarrier at offset `bar` receives the byte count.
+__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* map,
+                                                      uint32_t bar, int32_t x, int32_t y,
+                                                      uint16_t cta_mask)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(map), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
+        : "memory");
+}
+
+// ------------------------------------------------------------------------------------
+// Thread-block clusters
+// ------------------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA in the cluster: release own prior memory operations, then wait for
+// all CTAs of the cluster and acquire theirs.
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Plain (untiled) bulk copy of `bytes` (a multiple of 16) from global memory into shared memory;
+// both addresses 16-byte aligned.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// Orders this thread's generic-proxy shared-memory accesses before later async-proxy (TMA)
+// accesses of the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 // ------------------------------------------------------------------------------------
@@ -136,27 +199,103 @@ __device__ __forceinline__ void mma_commit(uint32_t bar)
         : "memory");
 }
 
+// Arrives once on the mbarrier at offset `bar` of every CTA in `cta_mask` when the tcgen05.mma
+// issued so far by this thread have completed.
+__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar), "h"(cta_mask)
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_ld()
 {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// 32 lanes x 32 consecutive 32-bit columns: thread t of the warp gets lane (base lane + t),
-// columns [col, col + 32) in r[0..31].
-__device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32])
+// tcgen05.wait::ld that also names the destination registers of the load it completes, so the
+// compiler cannot move any use of them above the wait.
+__device__ __forceinline__ void tmem_wait_ld(uint64_t (&r)[16])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+l"(r[0]), "+l"(r[1]), "+l"(r[2]), "+l"(r[3]), "+l"(r[4]), "+l"(r[5]),
+                   "+l"(r[6]), "+l"(r[7]), "+l"(r[8]), "+l"(r[9]), "+l"(r[10]), "+l"(r[11]),
+                   "+l"(r[12]), "+l"(r[13]), "+l"(r[14]), "+l"(r[15])
+                 :
+                 : "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns, returned as 16 packed pairs: r[i] holds columns
+// 2i (low half) and 2i + 1 (high half) of this thread's lane.
+__device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint64_t (&r)[16])
 {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32"
-        " {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-          "=r"(r[31])
+        "{\n .reg .b32 t<32>;\n"
+        " tcgen05.ld.sync.aligned.32x32b.x32.b32"
+        " {t0,t1,t2,t3,t4,t5,t6,t7,t8,t9,t10,t11,t12,t13,t14,t15,"
+        "t16,t17,t18,t19,t20,t21,t22,t23,t24,t25,t26,t27,t28,t29,t30,t31}, [%16];\n"
+        " mov.b64 %0, {t0, t1};\n mov.b64 %1, {t2, t3};\n mov.b64 %2, {t4, t5};\n"
+        " mov.b64 %3, {t6, t7};\n mov.b64 %4, {t8, t9};\n mov.b64 %5, {t10, t11};\n"
+        " mov.b64 %6, {t12, t13};\n mov.b64 %7, {t14, t15};\n mov.b64 %8, {t16, t17};\n"
+        " mov.b64 %9, {t18, t19};\n mov.b64 %10, {t20, t21};\n mov.b64 %11, {t22, t23};\n"
+        " mov.b64 %12, {t24, t25};\n mov.b64 %13, {t26, t27};\n mov.b64 %14, {t28, t29};\n"
+        " mov.b64 %15, {t30, t31};\n}"
+        : "=l"(r[0]), "=l"(r[1]), "=l"(r[2]), "=l"(r[3]), "=l"(r[4]), "=l"(r[5]), "=l"(r[6]),
+          "=l"(r[7]), "=l"(r[8]), "=l"(r[9]), "=l"(r[10]), "=l"(r[11]), "=l"(r[12]),
+          "=l"(r[13]), "=l"(r[14]), "=l"(r[15])
         : "r"(taddr)
         : "memory");
+}
+
+// tcgen05.wait::ld naming the 8 packed destination pairs of a 16-column load.
+__device__ __forceinline__ void tmem_wait_ld(uint64_t (&r)[8])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+l"(r[0]), "+l"(r[1]), "+l"(r[2]), "+l"(r[3]), "+l"(r[4]), "+l"(r[5]),
+                   "+l"(r[6]), "+l"(r[7])
+                 :
+                 : "memory");
+}
+
+// 32 lanes x 16 consecutive 32-bit columns as 8 packed pairs (columns 2i, 2i + 1 in r[i]).
+__device__ __forceinline__ void tmem_ld_16cols(uint32_t taddr, uint64_t (&r)[8])
+{
+    asm volatile(
+        "{\n .reg .b32 t<16>;\n"
+        " tcgen05.ld.sync.aligned.32x32b.x16.b32"
+        " {t0,t1,t2,t3,t4,t5,t6,t7,t8,t9,t10,t11,t12,t13,t14,t15}, [%8];\n"
+        " mov.b64 %0, {t0, t1};\n mov.b64 %1, {t2, t3};\n mov.b64 %2, {t4, t5};\n"
+        " mov.b64 %3, {t6, t7};\n mov.b64 %4, {t8, t9};\n mov.b64 %5, {t10, t11};\n"
+        " mov.b64 %6, {t12, t13};\n mov.b64 %7, {t14, t15};\n}"
+        : "=l"(r[0]), "=l"(r[1]), "=l"(r[2]), "=l"(r[3]), "=l"(r[4]), "=l"(r[5]), "=l"(r[6]),
+          "=l"(r[7])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Two FP32 lanes packed in 64 bits: the value (s, s).
+__device__ __forceinline__ uint64_t f32x2_splat(float s)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(s));
+    return r;
+}
+
+// acc = fma(p, s2, acc) on packed FP32 pairs: two IEEE round-to-nearest fused multiply-adds.
+__device__ __forceinline__ void ffma2(uint64_t& acc, uint64_t p, uint64_t s2)
+{
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(p), "l"(s2));
+}
+
+__device__ __forceinline__ float f32x2_lo(uint64_t v)
+{
+    return __uint_as_float(static_cast<uint32_t>(v));
+}
+
+__device__ __forceinline__ float f32x2_hi(uint64_t v)
+{
+    return __uint_as_float(static_cast<uint32_t>(v >> 32));
 }
 
 // Shared-memory matrix descriptor for a K-major operand tile whose rows are 128 bytes long and

@@ -14,6 +14,7 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace fp8bs {
 
@@ -96,55 +97,206 @@ __device__ __forceinline__ void st_v2(void* p, const uint2& v)
 }
 
 // ------------------------------------------------------------------------------------
-// 1x128 activation tiles.
-// A half-warp (16 lanes x 8 BF16 = 128 values) owns one tile; each half-warp task covers
-// TILES_PER_TASK consecutive tiles of one row, so a lane keeps that many 16-byte loads in
-// flight. Tasks are numbered row-major, so a warp reads 2 x TILES_PER_TASK x 256 contiguous
-// bytes. The loop runs per warp so that every shuffle sees all 32 lanes.
+// 1x128 activation tiles: persistent CTAs, TMA-staged, one tile per lane.
+//
+// The rows are cut into segments of up to 32 tiles (8 KB of BF16) of one row; each CTA owns a
+// contiguous, balanced range of segments. Segment i of a CTA belongs to consumer warp i % QA_CONSUMERS,
+// which owns QA_SLOTS_PER_WARP shared-memory slots and consumes them strictly in order (so every
+// slot's mbarriers see one producer and one consumer, phase after phase). A producer thread
+// streams the segments, in order, into the slots with bulk copies (QA_SLOTS x 8 KB in flight
+// per CTA). A consumer warp takes a whole segment: lane l loads tile l (16 x 16 B, rotated so that the reads are free of
+// bank conflicts), reduces its amax with packed 16-bit integer maxima on |bits| (exact for
+// finite BF16), computes its scale and reciprocal (one division pass covers 32 tiles), and
+// encodes its 128 values. The codes are written back into the slot and then copied out with
+// coalesced 16-byte stores (512 contiguous bytes per warp instruction).
 // ------------------------------------------------------------------------------------
-constexpr int TILES_PER_TASK = 4;
+constexpr int SEG_TILES = 32;
+constexpr int SEG_BYTES = SEG_TILES * 256;
+constexpr int QA_CONSUMERS = 6;
+constexpr int QA_SLOTS_PER_WARP = 2;
+constexpr int QA_SLOTS = QA_CONSUMERS * QA_SLOTS_PER_WARP;
+constexpr int QA_THREADS = (QA_CONSUMERS + 1) * 32;
+constexpr int QA_CTAS_PER_SM = 2;
+constexpr int QA_SMEM = QA_SLOTS * SEG_BYTES + 2 * QA_SLOTS * 8 + 16 + 128;
 
-__global__ void __launch_bounds__(QUANT_THREADS)
-quant_act_1x128_kernel(const uint16_t* __restrict__ x, int64_t M, int KB, int64_t ldx,
-                       uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ scales)
+struct QuantActArgs {
+    const uint16_t* x;
+    int64_t M;
+    int KB;
+    int64_t ldx;
+    uint8_t* q;
+    int64_t ldq;
+    float* scales;
+    int* err;
+    long long budget;
+};
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
 {
-    const int n_task_per_row = (KB + TILES_PER_TASK - 1) / TILES_PER_TASK;
-    const int64_t T = M * n_task_per_row;
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_shared_v2(uint32_t addr, const uint2& v)
+{
+    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(v.x), "r"(v.y) : "memory");
+}
+
+__device__ __forceinline__ void st_global_v4(void* p, const uint4& v)
+{
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// max |x| over eight BF16 values held as four 32-bit words: for finite BF16 the magnitude order
+// is the unsigned order of the bits with the sign cleared.
+__device__ __forceinline__ uint32_t absmax_bits_u16x2(const uint4& v, uint32_t m)
+{
+    m = max_u16x2(m, v.x & 0x7FFF7FFFu);
+    m = max_u16x2(m, v.y & 0x7FFF7FFFu);
+    m = max_u16x2(m, v.z & 0x7FFF7FFFu);
+    return max_u16x2(m, v.w & 0x7FFF7FFFu);
+}
+
+// Slot and barrier phase of a CTA's i-th segment: consumer warp w = i % QA_CONSUMERS handles
+// its k-th segment (k = i / QA_CONSUMERS) in its own slot w * QA_SLOTS_PER_WARP +
+// k % QA_SLOTS_PER_WARP, which it has used k / QA_SLOTS_PER_WARP times before.
+__device__ __forceinline__ uint32_t qa_slot(int64_t i)
+{
+    const int64_t w = i % QA_CONSUMERS, k = i / QA_CONSUMERS;
+    return static_cast<uint32_t>(w * QA_SLOTS_PER_WARP + k % QA_SLOTS_PER_WARP);
+}
+
+__device__ __forceinline__ uint32_t qa_phase(int64_t i)
+{
+    return static_cast<uint32_t>((i / QA_CONSUMERS) / QA_SLOTS_PER_WARP) & 1u;
+}
+
+__global__ void __launch_bounds__(QA_THREADS, QA_CTAS_PER_SM)
+quant_act_1x128_kernel(const QuantActArgs p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 127u) & ~127u;
+    const uint32_t bar_full = base + QA_SLOTS * SEG_BYTES;
+    const uint32_t bar_empty = bar_full + 8 * QA_SLOTS;
+    const uint32_t abort_addr = bar_empty + 8 * QA_SLOTS;   // shared word: a role gave up
+
+    const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int half = lane >> 4;
-    const int hl = lane & 15;
-    const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int KB = p.KB;
+    const int segs_per_row = (KB + SEG_TILES - 1) / SEG_TILES;
+    const int64_t total = p.M * segs_per_row;
+    const int64_t s_begin = total * blockIdx.x / gridDim.x;
+    const int64_t nseg = total * (blockIdx.x + 1) / gridDim.x - s_begin;
 
-    for (int64_t tw = warp0; 2 * tw < T; tw += nwarps) {
-        const int64_t t = 2 * tw + half;
-        const bool tv = t < T;
-        const int64_t m = tv ? t / n_task_per_row : 0;
-        const int kb0 = tv ? static_cast<int>(t % n_task_per_row) * TILES_PER_TASK : 0;
-
-        uint4 v[TILES_PER_TASK];
-#pragma unroll
-        for (int i = 0; i < TILES_PER_TASK; i++) {
-            const bool ok = tv && (kb0 + i < KB);
-            v[i] = ok ? ld_stream_v4(x + m * ldx + static_cast<int64_t>(kb0 + i) * 128 + hl * 8)
-                      : make_uint4(0u, 0u, 0u, 0u);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < QA_SLOTS; i++) {
+            mbar_init(bar_full + 8 * i, 1);
+            mbar_init(bar_empty + 8 * i, 1);
         }
-#pragma unroll
-        for (int i = 0; i < TILES_PER_TASK; i++) {
-            const bool ok = tv && (kb0 + i < KB);
-            float f[8];
-            unpack_bf16x8(v[i], f);
-            float a = absmax8(f);
-            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 8));
-            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 4));
-            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 2));
-            a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, 1));
-            const TileScale ts = tile_scale(a);
-            const uint2 codes = encode8(f, ts);
-            if (ok) {
-                st_v2(q + m * ldq + static_cast<int64_t>(kb0 + i) * 128 + hl * 8, codes);
-                if (hl == 0) scales[static_cast<int64_t>(kb0 + i) * M + m] = ts.s;
+        st_shared_volatile_u32(abort_addr, 0u);
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == QA_CONSUMERS) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int64_t i = 0;
+            bool ok = true;
+            for (; i < nseg; i++) {
+                const uint32_t slot = qa_slot(i);
+                const uint32_t ph = qa_phase(i);
+                if (!mbar_wait(bar_empty + 8 * slot, ph ^ 1u, abort_addr, p.budget)) {
+                    st_shared_volatile_u32(abort_addr, 1u);
+                    atomicCAS(p.err, 0, DEV_TIMEOUT_PRODUCER);
+                    ok = false;
+                    break;
+                }
+                const int64_t seg = s_begin + i;
+                const int64_t row = seg / segs_per_row;
+                const int tile0 = static_cast<int>(seg % segs_per_row) * SEG_TILES;
+                const int nt = min(SEG_TILES, KB - tile0);
+                const uint32_t bytes = static_cast<uint32_t>(nt) * 256u;
+                mbar_arrive_expect_tx(bar_full + 8 * slot, bytes);
+                bulk_load(base + slot * SEG_BYTES, p.x + row * p.ldx + static_cast<int64_t>(tile0) * 128,
+                          bytes, bar_full + 8 * slot);
             }
+            if (!ok) {
+                // wait for the copies already issued before the CTA exits
+                for (int64_t j = (i > QA_SLOTS ? i - QA_SLOTS : 0); j < i; j++)
+                    if (!mbar_wait(bar_full + 8 * qa_slot(j), qa_phase(j), 0u, p.budget))
+                        atomicCAS(p.err, 0, DEV_TIMEOUT_DRAIN);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ consumers
+        for (int64_t i = warp; i < nseg; i += QA_CONSUMERS) {
+            const uint32_t slot = qa_slot(i);
+            const uint32_t ph = qa_phase(i);
+            const bool got = mbar_wait(bar_full + 8 * slot, ph, abort_addr, p.budget);
+            if (!__all_sync(0xffffffffu, got)) {
+                if (lane == 0) {
+                    st_shared_volatile_u32(abort_addr, 1u);
+                    atomicCAS(p.err, 0, DEV_TIMEOUT_EPILOGUE);
+                }
+                break;
+            }
+            const int64_t seg = s_begin + i;
+            const int64_t row = seg / segs_per_row;
+            const int tile0 = static_cast<int>(seg % segs_per_row) * SEG_TILES;
+            const int nt = min(SEG_TILES, KB - tile0);
+            const bool active = lane < nt;
+            const uint32_t slot_base = base + slot * SEG_BYTES;
+            const uint32_t my_tile = slot_base + lane * 256;
+
+            uint4 v[16];
+#pragma unroll
+            for (int j = 0; j < 16; j++) {
+                const int c = (j + lane) & 15;
+                v[j] = active ? ld_shared_v4(my_tile + c * 16) : make_uint4(0u, 0u, 0u, 0u);
+            }
+            uint32_t m2 = 0;
+#pragma unroll
+            for (int j = 0; j < 16; j++) m2 = absmax_bits_u16x2(v[j], m2);
+            const uint32_t mbits = max(m2 & 0xFFFFu, m2 >> 16);
+            const TileScale ts = tile_scale(__uint_as_float(mbits << 16));
+            __syncwarp();   // every lane holds its tile before the codes overwrite the slot
+
+#pragma unroll
+            for (int j = 0; j < 16; j++) {
+                const int c = (j + lane) & 15;
+                float f[8];
+                unpack_bf16x8(v[j], f);
+                const uint2 codes = encode8(f, ts);
+                if (active) st_shared_v2(slot_base + lane * 128 + c * 8, codes);
+            }
+            __syncwarp();
+
+            const int code_bytes = nt * 128;
+            uint8_t* qrow = p.q + row * p.ldq + static_cast<int64_t>(tile0) * 128;
+#pragma unroll
+            for (int j = 0; j < SEG_TILES * 128 / 512; j++) {
+                const int off = j * 512 + lane * 16;
+                if (off < code_bytes) st_global_v4(qrow + off, ld_shared_v4(slot_base + off));
+            }
+            if (active) p.scales[static_cast<int64_t>(tile0 + lane) * p.M + row] = ts.s;
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
         }
     }
 }
@@ -204,16 +356,26 @@ quant_weight_128x128_kernel(const uint16_t* __restrict__ w, int64_t N, int KB, i
 }  // namespace
 
 cudaError_t launch_quant_act(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
-                             int64_t ldq, float* scales, int num_sms, cudaStream_t stream)
+                             int64_t ldq, float* scales, int num_sms, int* err, long long budget,
+                             cudaStream_t stream)
 {
-    const int KB = static_cast<int>(K / 128);
-    const int64_t tasks = M * ((KB + TILES_PER_TASK - 1) / TILES_PER_TASK);
-    const int64_t warps = (tasks + 1) / 2;
-    const int64_t want = (warps + QUANT_THREADS / 32 - 1) / (QUANT_THREADS / 32);
-    const int64_t cap = static_cast<int64_t>(num_sms) * (2048 / QUANT_THREADS);
-    const int grid = static_cast<int>(want < cap ? want : cap);
-    quant_act_1x128_kernel<<<grid, QUANT_THREADS, 0, stream>>>(
-        static_cast<const uint16_t*>(x), M, KB, ldx, q, ldq, scales);
+    QuantActArgs a;
+    a.x = static_cast<const uint16_t*>(x);
+    a.M = M;
+    a.KB = static_cast<int>(K / 128);
+    a.ldx = ldx;
+    a.q = q;
+    a.ldq = ldq;
+    a.scales = scales;
+    a.err = err;
+    a.budget = budget;
+    const int64_t segs = M * ((a.KB + SEG_TILES - 1) / SEG_TILES);
+    const int64_t cap = static_cast<int64_t>(num_sms) * QA_CTAS_PER_SM;
+    const int grid = static_cast<int>(segs < cap ? segs : cap);
+    cudaError_t e = cudaFuncSetAttribute(quant_act_1x128_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, QA_SMEM);
+    if (e != cudaSuccess) return e;
+    quant_act_1x128_kernel<<<grid, QA_THREADS, QA_SMEM, stream>>>(a);
     return cudaGetLastError();
 }
 
