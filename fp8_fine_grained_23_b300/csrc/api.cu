@@ -13,16 +13,10 @@
 #include "internal.h"
 
 using namespace fp8bs;
+using namespace fp8bs::host;
 
-namespace {
-
-constexpr int MAX_DEVICES = 64;
-
-struct DeviceInfo {
-    int checked = 0;      // 0 unknown, 1 sm_103, -1 other
-    int num_sms = 0;
-    int* err = nullptr;   // device error word (allocated on first GEMM call)
-};
+namespace fp8bs {
+namespace host {
 
 std::mutex g_mu;
 DeviceInfo g_dev[MAX_DEVICES];
@@ -39,8 +33,6 @@ long long wait_budget()
     return budget;
 }
 
-inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
 // Current device, checked to be compute capability 10.3; fills *info.
 int current_device(DeviceInfo** info)
@@ -146,9 +138,8 @@ int check_gemm_args(const void* a_q, const void* a_s, const void* w_q, const voi
     return FP8BS_OK;
 }
 
-inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? FP8BS_OK : FP8BS_ERR_CUDA; }
-
-}  // namespace
+}  // namespace host
+}  // namespace fp8bs
 
 extern "C" {
 

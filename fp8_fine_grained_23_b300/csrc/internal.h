@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
+#include "fp8bs.h"
+
 namespace fp8bs {
 
 constexpr int QUANT_THREADS = 256;
@@ -55,5 +57,35 @@ cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, cons
                         bool grouped, bool out_f32, int max_ctas, cudaStream_t stream);
 int gemm_cluster_size(bool grouped);
 size_t gemm_smem_bytes(bool grouped, int G);
+
+// ------------------------------------------------------------------------------------
+// Host-side helpers of the C ABI (api.cu)
+// ------------------------------------------------------------------------------------
+namespace host {
+
+constexpr int MAX_DEVICES = 64;
+
+struct DeviceInfo {
+    int checked = 0;      // 0 unknown, 1 sm_103, -1 other
+    int num_sms = 0;
+    int* err = nullptr;   // device error word (allocated on first use)
+};
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? FP8BS_OK : FP8BS_ERR_CUDA; }
+
+long long wait_budget();
+int current_device(DeviceInfo** info);
+int ensure_error_word(DeviceInfo* d);
+int ensure_encoder();
+int make_code_map(CUtensorMap* map, const void* base, int64_t cols, int64_t rows, int64_t ld,
+                  int box_rows);
+int check_quant_args(const void* in, int64_t rows, int64_t K, int64_t ld_in, const void* q,
+                     int64_t ldq, const void* scales);
+int check_gemm_args(const void* a_q, const void* a_s, const void* w_q, const void* w_s,
+                    int64_t rows, int64_t N, int64_t K, const void* c, int64_t ldc, int out_dtype);
+
+}  // namespace host
 
 }  // namespace fp8bs

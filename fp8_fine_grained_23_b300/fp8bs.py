@@ -25,13 +25,16 @@ _i64, _p, _int = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
 lib.fp8_quant_act_1x128.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p, _p]
 lib.fp8_quant_weight_128x128.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p, _p]
 lib.fp8_blockscaled_gemm.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, _p, _i64, _int, _p]
+lib.fp8_blockscaled_gemm_noalloc.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, _p, _i64, _int,
+                                             _p]
 lib.fp8_blockscaled_grouped_gemm.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _p,
                                              _i64, _int, _p]
 lib.fp8bs_status_string.argtypes = [_int]
 lib.fp8bs_status_string.restype = ctypes.c_char_p
 lib.fp8bs_last_error.argtypes = [_p]
 for _f in (lib.fp8_quant_act_1x128, lib.fp8_quant_weight_128x128, lib.fp8_blockscaled_gemm,
-           lib.fp8_blockscaled_grouped_gemm, lib.fp8bs_last_error):
+           lib.fp8_blockscaled_gemm_noalloc, lib.fp8_blockscaled_grouped_gemm,
+           lib.fp8bs_last_error):
     _f.restype = _int
 
 FP8BS_OK = 0
@@ -130,6 +133,21 @@ def fp8_blockscaled_gemm(a_q: torch.Tensor, a_s: torch.Tensor, w_q: torch.Tensor
            lib.fp8_blockscaled_gemm(a_q.data_ptr(), a_s.data_ptr(), w_q.data_ptr(),
                                     w_s.data_ptr(), M, N, K, out.data_ptr(), ldc,
                                     _out_code(out.dtype), _stream(stream)))
+    return out
+
+
+def fp8_blockscaled_gemm_noalloc(a_q: torch.Tensor, a_s: torch.Tensor, w_q: torch.Tensor,
+                                 w_s: torch.Tensor, out: torch.Tensor, stream=None) -> torch.Tensor:
+    """fp8_blockscaled_gemm for callers that must not allocate device memory: the library uses a
+    fixed scratch word inside its own image instead of allocating one. `out` is required (this
+    wrapper allocates nothing either). Calls that may overlap on the GPU must be ordered."""
+    M, K = a_q.shape
+    N = w_q.shape[0]
+    _, ldc = _rows_ld(out, "out")
+    _check("fp8_blockscaled_gemm_noalloc",
+           lib.fp8_blockscaled_gemm_noalloc(a_q.data_ptr(), a_s.data_ptr(), w_q.data_ptr(),
+                                            w_s.data_ptr(), M, N, K, out.data_ptr(), ldc,
+                                            _out_code(out.dtype), _stream(stream)))
     return out
 
 

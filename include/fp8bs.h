@@ -119,7 +119,7 @@ int fp8_blockscaled_gemm(const uint8_t *a_q, const float *a_s,
  *                  outside [0, R] or decreasing are outside the contract (no hang; the rows
  *                  written are unspecified).
  *   c              [R][ldc] BF16 or FP32.
- * Requires G in [1, 4096], R >= 0 (R == 0 is a no-op), plus the dense call's rules for N, K,
+ * Requires G in [1, 1024], R >= 0 (R == 0 is a no-op), plus the dense call's rules for N, K,
  * ldc and alignment. Empty groups are allowed.
  */
 int fp8_blockscaled_grouped_gemm(const uint8_t *a_q, const float *a_s,
@@ -127,6 +127,36 @@ int fp8_blockscaled_grouped_gemm(const uint8_t *a_q, const float *a_s,
                                  const int32_t *group_offsets, int64_t G, int64_t R,
                                  int64_t N, int64_t K, void *c, int64_t ldc, int out_dtype,
                                  fp8bs_stream_t stream);
+
+/*
+ * fp8_blockscaled_gemm_noalloc: the same dense block-scaled GEMM as fp8_blockscaled_gemm, for
+ * callers that cannot let a library allocate device memory. The pages describe no such interface;
+ * this entry point has no counterpart there.
+ *
+ * Who needs it: code that runs while a CUDA graph is captured in a mode that forbids allocation,
+ * runtimes that own all device memory through their own pool and forbid other cudaMalloc calls,
+ * and deployments that must fix their device footprint before they start. fp8_blockscaled_gemm
+ * allocates a 4-byte error word with cudaMalloc on its first call on a device; this variant never
+ * calls cudaMalloc, cudaFree or any allocating routine.
+ *
+ * Instead its kernel keeps that scratch word in a fixed 256-byte array inside the library image
+ * (a static __device__ array: every GPU that loads the library holds it until the process exits).
+ * A call needs one 4-byte word of it for any problem size; a call that would need more than the
+ * array holds is rejected with FP8BS_ERR_INVALID_ARG before anything is launched.
+ *
+ * The first call on a device looks up the array's device address (once per device, with that
+ * device current); make that first call before any stream capture begins. Every call clears the
+ * word on `stream` before its launch, and every call shares the same array: calls that can
+ * overlap on the GPU (different streams without ordering between them) race on it, so order them.
+ * A pipeline timeout of this variant is recorded in that shared word, which fp8bs_last_error()
+ * does not read; callers that need that status use fp8_blockscaled_gemm.
+ *
+ * Arguments, layouts, requirements and results are exactly those of fp8_blockscaled_gemm.
+ */
+int fp8_blockscaled_gemm_noalloc(const uint8_t *a_q, const float *a_s,
+                                 const uint8_t *w_q, const float *w_s,
+                                 int64_t M, int64_t N, int64_t K,
+                                 void *c, int64_t ldc, int out_dtype, fp8bs_stream_t stream);
 
 /* Human-readable name of a status code. The string is static. */
 const char *fp8bs_status_string(int status);
