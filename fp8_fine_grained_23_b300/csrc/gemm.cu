@@ -10,26 +10,36 @@
 // drain it, which overlaps with the MMAs of the next K block.
 //
 // Structure of one persistent CTA (384 threads = 3 warpgroups, one CTA per SM):
-//   warp 0     TMA producer: streams 128x128 A and 256x128 W code tiles into a STAGES-deep
-//              shared-memory ring (128-byte swizzle), completion tracked by mbarriers;
-//   warp 1     TMEM owner and MMA issuer: for each K block, four tcgen05.mma (K = 32 each,
-//              kind::f8f6f4, E4M3 x E4M3 -> FP32) into one of two 128x256 TMEM accumulators,
-//              then tcgen05.commit to free the smem stage and to hand the partial to the
+//   warp 0     TMA producer: streams the CTA's 128x128 A code tile and its part of the W code
+//              tile into a shared-memory ring (128-byte swizzle), completion on mbarriers;
+//   warp 1     TMEM owner and MMA issuer: per K block, four tcgen05.mma (K = 32 each,
+//              kind::f8f6f4, E4M3 x E4M3 -> FP32) into one of two TMEM accumulators, then
+//              tcgen05.commit to free the shared-memory stage and to hand the partial to the
 //              epilogue;
-//   warps 2-3  idle after set-up (warp 0 also builds the group table of the grouped variant);
-//   warps 4-11 epilogue: warp w reads TMEM lanes 32*(w%4).. (its rows) and columns
-//              128*((w-4)/4).. (one weight block), promotes each K block's partial into 128
-//              FP32 registers per thread (packed pairs, fma.rn.f32x2), and writes the
-//              finished tile (BF16 or FP32).
-// Dense GEMMs run as clusters of two CTAs on adjacent m-tiles of the same n-tile: each CTA loads
-// its own A tile and one half (128 rows) of the shared W tile, multicast into both CTAs' shared
-// memory, which cuts the L2-to-SM traffic per K block from 48 KB to 32 KB per CTA. A stage is
-// free again only when both CTAs' MMAs have read it, so each MMA commit is multicast to the
-// empty barriers of both CTAs (count 2). A cluster barrier after set-up and before exit keeps
-// every remote arrival and multicast write inside both CTAs' lifetimes.
+//   warp 2     scale loader: per K block, cp.async copies of the tile's 128 activation scales
+//              and its two weight-block scales into an 8-slot shared-memory ring (sfull/sempty
+//              mbarriers), so the epilogue reads its scale from shared memory;
+//   warp 3     idle after set-up (warp 0 also builds the group table of the grouped variant);
+//   warps 4-11 epilogue: warp w reads TMEM lanes 32*(w%4).. (its rows) and the 128 columns
+//              128*((w-4)/4).. (one weight block). Per K block it loads the partial in 32-column
+//              pieces (the next piece in flight while the current one is promoted) and promotes
+//              it into 128 FP32 registers per thread (packed pairs, fma.rn.f32x2). At the end of
+//              the tile the results go through a small shared-memory stage per warp and leave as
+//              whole 64-byte row segments (BF16 or FP32).
+//
+// The dense GEMM runs on CTA pairs (clusters of two, cta_group::2): the pair computes a 256x256
+// tile with one 256-row MMA per K step, issued by the even CTA. Each CTA loads only its own 128
+// A rows and 128 of the 256 W rows, so a K block brings 32 KB into each SM instead of 48 KB, and
+// a stage takes 32 KB, which leaves room for six. Both CTAs' loads complete on the even CTA's
+// `full` barrier; the MMA commits are multicast to both CTAs' `empty` and `tfull` barriers. Each
+// CTA's epilogue releases its local `tempty` barrier; the odd CTA's MMA warp, otherwise idle,
+// forwards each release to the even CTA's `tempty`, keeping the slow cross-CTA arrive off the
+// epilogue's path. The grouped GEMM, which is bound
+// by streaming expert weights from HBM, keeps single-CTA MMAs on 128x256 tiles.
+//
 // Registers: the launch gives 168 per thread (65536 / 384, rounded to 8). Warpgroup 0 drops to
-// 56 and the two epilogue warpgroups rise to 224 (128*56 + 256*224 = 384*168), which holds the
-// 128 accumulators and 32 staging registers of an epilogue thread.
+// 72 and the two epilogue warpgroups rise to 216 (128*72 + 256*216 = 384*168), which holds the
+// 128 accumulators and 64 staging registers of an epilogue thread.
 // Every mbarrier wait is bounded (clock budget); on expiry the CTA records an error code in the
 // device error word, stops issuing work, waits for its in-flight copies and MMAs, frees TMEM and
 // returns.
@@ -48,36 +58,41 @@ constexpr int BK = GEMM_BK;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int PRODUCER_WARP = 0;
 constexpr int MMA_WARP = 1;
+constexpr int SCALE_WARP = 2;
 constexpr int EPI_WARP0 = 4;
 constexpr int THREADS = 384;
-constexpr int REGS_CONTROL = 56;           // warpgroup 0 after setmaxnreg.dec
-constexpr int REGS_EPILOGUE = 224;         // warpgroups 1 and 2 after setmaxnreg.inc
+constexpr int REGS_CONTROL = 72;           // warpgroup 0 after setmaxnreg.dec
+constexpr int REGS_EPILOGUE = 216;         // warpgroups 1 and 2 after setmaxnreg.inc
 static_assert(128 * REGS_CONTROL + 256 * REGS_EPILOGUE == THREADS * 168,
               "register split must equal the launch allocation of 168 per thread");
 constexpr int TMEM_COLS = 2 * BN;          // two FP32 accumulators of 128 lanes x BN columns
 
 constexpr int A_BYTES = BM * BK;           // E4M3: one byte per element
-constexpr int B_BYTES = BN * BK;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int STG_WARP_BYTES = 32 * 128;   // output staging per epilogue warp: 32 rows x 128 B
+constexpr int B_BYTES = BN * BK;           // the whole W tile
+constexpr int STG_WARP_BYTES = 32 * 64;    // output staging per epilogue warp: 32 rows x 64 B
 constexpr int STG_BYTES = NUM_EPI_WARPS * STG_WARP_BYTES;
+constexpr int SCALE_SLOTS = 8;             // scale ring: one slot per K block in flight
+constexpr int SCALE_SLOT_BYTES = 528;      // 128 activation scales + 2 weight scales, padded
 constexpr int ALIGN_PAD = 1024;            // 128-byte-swizzled tiles need 1024-byte alignment
 
-// Shared-memory layout. The dense kernel keeps four 48 KB stages; the grouped kernel, which is
-// bound by streaming expert weights from HBM, keeps three and leaves room for its group table.
-template <bool GROUPED>
+// Shared-memory layout per CTA. PAIR: a CTA holds its A tile and half of the W tile.
+template <bool GROUPED, bool PAIR>
 struct Layout {
-    static constexpr int STAGES = GROUPED ? 3 : 4;
+    static constexpr int CL = PAIR ? 2 : 1;              // CTAs per cluster
+    static constexpr int B_PART = B_BYTES / CL;          // W rows held by this CTA
+    static constexpr int STAGE = A_BYTES + B_PART;
+    static constexpr int STAGES = PAIR ? 6 : (GROUPED ? 3 : 4);
     static constexpr int A_OFF = 0;
     static constexpr int B_OFF = STAGES * A_BYTES;
-    static constexpr int STG_OFF = STAGES * STAGE_BYTES;
-    static constexpr int BAR_OFF = STG_OFF + STG_BYTES;
-    static constexpr int NUM_BARS = 2 * STAGES + 5;   // full[S], empty[S], tfull[2], tempty[2], drain
+    static constexpr int STG_OFF = STAGES * STAGE;
+    static constexpr int SCL_OFF = STG_OFF + STG_BYTES;
+    static constexpr int BAR_OFF = SCL_OFF + SCALE_SLOTS * SCALE_SLOT_BYTES;
+    // full[S], empty[S], tfull[2], tempty[2], drain, sfull[SCALE_SLOTS], sempty[SCALE_SLOTS]
+    static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * SCALE_SLOTS;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int GROUP_OFF = MISC_OFF + 16;
+    static_assert(A_BYTES % 1024 == 0 && B_PART % 1024 == 0, "tiles keep 1024-byte alignment");
 };
-
-static_assert(A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "tiles must keep 1024-B alignment");
 
 struct TileInfo {
     int64_t row0;      // first row of the tile in A / C
@@ -93,18 +108,18 @@ __device__ __forceinline__ void raise_error(int* err, uint32_t abort_addr, int c
     atomicCAS(err, 0, code);
 }
 
-// Work item t of a CTA whose rank in its cluster is `crank`. Dense: t numbers groups of
-// CLUSTER adjacent m-tiles (one per CTA of the cluster) on one n-tile, m fastest; an m-tile past
-// the last row reads zeros and stores nothing. Grouped (CLUSTER == 1): t numbers
-// (group, n-tile, m-tile) with m fastest.
-template <bool GROUPED, int CLUSTER>
+// Work item t of a CTA whose rank in its cluster is `crank`. Dense: t numbers groups of CL
+// adjacent m-tiles (one per CTA of the cluster) on one n-tile, m fastest; an m-tile past the last
+// row reads zeros and stores nothing. Grouped (CL == 1): t numbers (group, n-tile, m-tile) with
+// m fastest, so the m-tiles of one expert's W tile run side by side.
+template <bool GROUPED, int CL>
 __device__ __forceinline__ TileInfo decode_tile(int t, const GemmArgs& p, const int* s_tstart,
                                                 const int* s_off, int crank)
 {
     TileInfo ti;
     if constexpr (!GROUPED) {
-        const int mgroups = (p.MT + CLUSTER - 1) / CLUSTER;
-        const int mt = (t % mgroups) * CLUSTER + crank;
+        const int mgroups = (p.MT + CL - 1) / CL;
+        const int mt = (t % mgroups) * CL + crank;
         const int nt = t / mgroups;
         ti.row0 = static_cast<int64_t>(mt) * BM;
         ti.row_end = p.rows;
@@ -122,7 +137,7 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const GemmArgs& p, const 
         const int local = t - s_tstart[g];
         const int rows_g = s_off[g + 1] - s_off[g];
         const int mtg = (rows_g + BM - 1) / BM;
-        const int nt = local / mtg;         // m-tiles of one (group, n-tile) are adjacent
+        const int nt = local / mtg;
         const int mt = local % mtg;
         ti.row0 = static_cast<int64_t>(s_off[g]) + static_cast<int64_t>(mt) * BM;
         const int64_t end = s_off[g + 1];
@@ -153,6 +168,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return r;
 }
 
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4& v)
 {
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
@@ -177,13 +199,14 @@ __device__ __forceinline__ void st_v4(void* p, uint32_t a, uint32_t b, uint32_t 
                  : "memory");
 }
 
-template <bool GROUPED, bool OUT_F32, int CLUSTER>
+template <bool GROUPED, bool OUT_F32, bool PAIR>
 __global__ void __launch_bounds__(THREADS, 1)
 fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                             const __grid_constant__ CUtensorMap map_b, const GemmArgs p)
 {
-    using L = Layout<GROUPED>;
+    using L = Layout<GROUPED, PAIR>;
     constexpr int STAGES = L::STAGES;
+    constexpr int CL = L::CL;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + (ALIGN_PAD - 1)) & ~static_cast<uint32_t>(ALIGN_PAD - 1);
@@ -197,30 +220,37 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     const uint32_t tfull0 = bar0 + 16 * STAGES;
     const uint32_t tempty0 = tfull0 + 16;
     const uint32_t drain_bar = tempty0 + 16;
+    const uint32_t sfull0 = drain_bar + 8;
+    const uint32_t sempty0 = sfull0 + 8 * SCALE_SLOTS;
+    const uint32_t scl0 = base + L::SCL_OFF;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
     const uint32_t abort_addr = base + L::MISC_OFF + 4;   // shared word: a role gave up
     int* s_tstart = reinterpret_cast<int*>(smem + L::GROUP_OFF);   // grouped: [G+1]
-    int* s_off = s_tstart + (p.G + 1);                            // grouped: [G+1]
+    int* s_off = s_tstart + (p.G + 1);                               // grouped: [G+1]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const long long budget = p.budget;
-    const int crank = CLUSTER > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-    const int cluster_id = blockIdx.x / CLUSTER;
-    const int num_clusters = gridDim.x / CLUSTER;
-    constexpr uint16_t CLUSTER_MASK = static_cast<uint16_t>((1u << CLUSTER) - 1u);
-    constexpr int B_PART = B_BYTES / CLUSTER;     // W rows loaded (and multicast) by each CTA
+    const uint32_t crank = PAIR ? cluster_ctarank() : 0u;
+    const bool leader = (crank & 1u) == 0u;   // the even CTA of a pair issues the pair's MMAs
+    const int cluster_id = blockIdx.x / CL;
+    const int num_clusters = gridDim.x / CL;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; s++) {
             mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, CLUSTER);   // one commit from every CTA of the cluster
+            mbar_init(empty0 + 8 * s, 1);
         }
         for (int b = 0; b < 2; b++) {
             mbar_init(tfull0 + 8 * b, 1);
-            mbar_init(tempty0 + 8 * b, NUM_EPI_WARPS);
+            // local epilogue warps, plus (even CTA of a pair) one forwarded arrive from the peer
+            mbar_init(tempty0 + 8 * b, NUM_EPI_WARPS + ((PAIR && leader) ? 1 : 0));
         }
         mbar_init(drain_bar, 1);
+        for (int i = 0; i < SCALE_SLOTS; i++) {
+            mbar_init(sfull0 + 8 * i, 32);              // one cp.async completion per loader lane
+            mbar_init(sempty0 + 8 * i, NUM_EPI_WARPS);
+        }
         st_shared_volatile_u32(abort_addr, 0u);
         fence_mbar_init();
     }
@@ -229,8 +259,13 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
         tma_prefetch_map(&map_b);
     }
     if (warp == MMA_WARP) {
-        tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(smem_u32(tmem_holder), TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     if constexpr (GROUPED) {
         // Group table: copy the offsets, then s_tstart[g] = sum over g' < g of
@@ -258,23 +293,26 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     }
     tc_fence_before();
     __syncthreads();
-    if constexpr (CLUSTER > 1) cluster_sync();   // peers' barriers exist before any multicast
+    if constexpr (PAIR) cluster_sync();   // the peer's barriers exist before anything targets them
     tc_fence_after();
 
     const uint32_t tmem_base = *tmem_holder;
     int num_tiles = p.num_tiles;
     if constexpr (GROUPED) num_tiles = s_tstart[p.G];
     const int KB = p.KB;
+    // The barriers the pair's MMA waits on live in the even CTA (rank crank & ~1).
 
     if (warp < EPI_WARP0) {
         regs_dec<REGS_CONTROL>();
         if (warp == PRODUCER_WARP) {
             // ---------------------------------------------------------------- TMA producer
             if (lane == 0) {
+                const uint32_t full_lead0 = PAIR ? mapa_shared(full0, crank & ~1u) : full0;
                 uint32_t it = 0;
                 bool ok = true;
                 for (int t = cluster_id; ok && t < num_tiles; t += num_clusters) {
-                    const TileInfo ti = decode_tile<GROUPED, CLUSTER>(t, p, s_tstart, s_off, crank);
+                    const TileInfo ti =
+                        decode_tile<GROUPED, CL>(t, p, s_tstart, s_off, static_cast<int>(crank));
                     for (int kb = 0; kb < KB; kb++, it++) {
                         const uint32_t s = it % STAGES;
                         const uint32_t ph = (it / STAGES) & 1u;
@@ -283,21 +321,24 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(full0 + 8 * s, STAGE_BYTES);
-                        tma_load_2d(sA + s * A_BYTES, &map_a, full0 + 8 * s, kb * BK,
-                                    static_cast<int32_t>(ti.row0));
-                        if constexpr (CLUSTER == 1) {
-                            tma_load_2d(sB + s * B_BYTES, &map_b, full0 + 8 * s, kb * BK,
-                                        static_cast<int32_t>(ti.wrow0));
+                        if constexpr (PAIR) {
+                            // the even CTA's barrier counts the bytes of both CTAs
+                            if (leader) mbar_arrive_expect_tx(full0 + 8 * s, CL * L::STAGE);
+                            tma_load_2d_pair(sA + s * A_BYTES, &map_a, full_lead0 + 8 * s, kb * BK,
+                                             static_cast<int32_t>(ti.row0));
+                            tma_load_2d_pair(sB + s * L::B_PART, &map_b, full_lead0 + 8 * s,
+                                             kb * BK,
+                                             static_cast<int32_t>(ti.wrow0 + crank * (BN / CL)));
                         } else {
-                            tma_load_2d_multicast(sB + s * B_BYTES + crank * B_PART, &map_b,
-                                                  full0 + 8 * s, kb * BK,
-                                                  static_cast<int32_t>(ti.wrow0 + crank * (BN / CLUSTER)),
-                                                  CLUSTER_MASK);
+                            mbar_arrive_expect_tx(full0 + 8 * s, L::STAGE);
+                            tma_load_2d(sA + s * A_BYTES, &map_a, full0 + 8 * s, kb * BK,
+                                        static_cast<int32_t>(ti.row0));
+                            tma_load_2d(sB + s * L::B_PART, &map_b, full0 + 8 * s, kb * BK,
+                                        static_cast<int32_t>(ti.wrow0));
                         }
                     }
                 }
-                if (!ok) {
+                if (!ok && leader) {
                     // The MMA side may never consume what is in flight: wait for the last copy
                     // issued into every stage before the CTA may exit.
                     const uint32_t first = it > STAGES ? it - STAGES : 0;
@@ -308,84 +349,161 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
             }
         } else if (warp == MMA_WARP) {
             // ---------------------------------------------------------------- MMA issuer
-            if (lane == 0) {
-                constexpr uint32_t IDESC = idesc_e4m3_f32(BM, BN);
+            if (lane == 0 && leader) {
+                constexpr uint32_t IDESC = idesc_e4m3_f32(BM * CL, BN);
+                constexpr uint16_t PAIR_MASK = 0x3;
                 uint32_t it = 0, j = 0;
                 bool ok = true, issued = false;
                 for (int t = cluster_id; ok && t < num_tiles; t += num_clusters) {
                     for (int kb = 0; kb < KB; kb++, it++, j++) {
                         const uint32_t b = j & 1u;
                         const uint32_t pb = (j >> 1) & 1u;
-                        if (!mbar_wait(tempty0 + 8 * b, pb ^ 1u, abort_addr, budget)) {
+                        const bool freed = mbar_wait(tempty0 + 8 * b, pb ^ 1u, abort_addr, budget);
+                        if (!freed) {
                             raise_error(p.err, abort_addr, DEV_TIMEOUT_MMA_TMEM);
                             ok = false;
                             break;
                         }
                         const uint32_t s = it % STAGES;
                         const uint32_t ph = (it / STAGES) & 1u;
-                        if (!mbar_wait(full0 + 8 * s, ph, abort_addr, budget)) {
+                        const bool filled = mbar_wait(full0 + 8 * s, ph, abort_addr, budget);
+                        if (!filled) {
                             raise_error(p.err, abort_addr, DEV_TIMEOUT_MMA_FULL);
                             ok = false;
                             break;
                         }
                         tc_fence_after();
                         const uint64_t da = desc_kmajor_sw128(sA + s * A_BYTES);
-                        const uint64_t db = desc_kmajor_sw128(sB + s * B_BYTES);
+                        const uint64_t db = desc_kmajor_sw128(sB + s * L::B_PART);
                         const uint32_t d_tmem = tmem_base + b * BN;
-    #pragma unroll
-                        for (int k = 0; k < BK / 32; k++)   // +32 bytes of K = +2 in the address field
-                            mma_e4m3(d_tmem, da + 2 * k, db + 2 * k, IDESC, k > 0 ? 1u : 0u);
-                        if constexpr (CLUSTER == 1) mma_commit(empty0 + 8 * s);
-                        else mma_commit_multicast(empty0 + 8 * s, CLUSTER_MASK);
-                        mma_commit(tfull0 + 8 * b);
+#pragma unroll
+                        for (int k = 0; k < BK / 32; k++) {   // +32 bytes of K = +2 in the address field
+                            if constexpr (PAIR)
+                                mma_e4m3_pair(d_tmem, da + 2 * k, db + 2 * k, IDESC, k > 0 ? 1u : 0u);
+                            else
+                                mma_e4m3(d_tmem, da + 2 * k, db + 2 * k, IDESC, k > 0 ? 1u : 0u);
+                        }
+                        if constexpr (PAIR) {
+                            mma_commit_pair_multicast(empty0 + 8 * s, PAIR_MASK);
+                            mma_commit_pair_multicast(tfull0 + 8 * b, PAIR_MASK);
+                        } else {
+                            mma_commit(empty0 + 8 * s);
+                            mma_commit(tfull0 + 8 * b);
+                        }
                         issued = true;
                     }
                 }
                 if (issued) {
                     // Every MMA must have finished before TMEM is released.
-                    mma_commit(drain_bar);
+                    if constexpr (PAIR)
+                        mma_commit_pair_multicast(drain_bar, static_cast<uint16_t>(1u << crank));
+                    else
+                        mma_commit(drain_bar);
                     if (!mbar_wait(drain_bar, 0, 0u, budget)) atomicCAS(p.err, 0, DEV_TIMEOUT_DRAIN);
+                }
+            } else if (PAIR && !leader && lane == 0) {
+                // Odd CTA of a pair: forward the release of each TMEM accumulator by this CTA's
+                // epilogue (its local tempty barrier) to the even CTA, whose MMA waits for both.
+                const uint32_t peer_tempty0 = mapa_shared(tempty0, crank & ~1u);
+                uint32_t j = 0;
+                bool ok = true;
+                for (int t = cluster_id; ok && t < num_tiles; t += num_clusters) {
+                    for (int kb = 0; kb < KB; kb++, j++) {
+                        const uint32_t b = j & 1u;
+                        if (!mbar_wait(tempty0 + 8 * b, (j >> 1) & 1u, abort_addr, budget)) {
+                            raise_error(p.err, abort_addr, DEV_TIMEOUT_MMA_TMEM);
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_cluster(peer_tempty0 + 8 * b);
+                    }
                 }
             }
             __syncwarp();
+        } else if (warp == SCALE_WARP) {
+            // ---------------------------------------------------------------- scale loader
+            // Slot it % SCALE_SLOTS receives the K block's 128 activation scales (rows of this
+            // CTA's tile; zero past the last row) and the scales of the tile's two weight blocks,
+            // by asynchronous copies whose completion arrives on sfull. The epilogue frees it.
+            uint32_t it = 0;
+            bool ok = true;
+            const float* zero_src = p.a_s;   // any valid address; zero-filled copies read nothing
+            for (int t = cluster_id; ok && t < num_tiles; t += num_clusters) {
+                const TileInfo ti =
+                    decode_tile<GROUPED, CL>(t, p, s_tstart, s_off, static_cast<int>(crank));
+                bool rv[4];
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    const int64_t row = ti.row0 + lane + 32 * q;
+                    rv[q] = row >= 0 && row < ti.row_end;
+                }
+                const int nb = ti.n0 / 128 + lane;           // lanes 0, 1: the two weight blocks
+                const bool wv = lane < 2 && nb < p.NB;
+                const float* w_base =
+                    p.w_s + (static_cast<int64_t>(ti.g) * p.NB + (wv ? nb : 0)) * KB;
+                for (int kb = 0; kb < KB; kb++, it++) {
+                    const uint32_t slot = it % SCALE_SLOTS;
+                    const uint32_t ph = (it / SCALE_SLOTS) & 1u;
+                    const bool got = mbar_wait(sempty0 + 8 * slot, ph ^ 1u, abort_addr, budget);
+                    if (!__all_sync(0xffffffffu, got)) {
+                        if (lane == 0) raise_error(p.err, abort_addr, DEV_TIMEOUT_SCALES);
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t dst = scl0 + slot * SCALE_SLOT_BYTES;
+                    const float* a_row = p.a_s + static_cast<int64_t>(kb) * p.rows + ti.row0;
+#pragma unroll
+                    for (int q = 0; q < 4; q++)
+                        cp_async_4(dst + (lane + 32 * q) * 4,
+                                   rv[q] ? a_row + lane + 32 * q : zero_src, rv[q] ? 4u : 0u);
+                    if (lane < 2)
+                        cp_async_4(dst + 512 + lane * 4, wv ? w_base + kb : zero_src, wv ? 4u : 0u);
+                    cp_async_mbar_arrive(sfull0 + 8 * slot);
+                }
+            }
+            // Copies still in flight complete on their own; wait for them before the CTA exits.
+            if (it > 0) {
+                const uint32_t first = it > SCALE_SLOTS ? it - SCALE_SLOTS : 0;
+                for (uint32_t i = first; i < it; i++)
+                    if (!mbar_wait(sfull0 + 8 * (i % SCALE_SLOTS), (i / SCALE_SLOTS) & 1u, 0u,
+                                   budget))
+                        atomicCAS(p.err, 0, DEV_TIMEOUT_DRAIN);
+            }
         }
     } else {
         regs_inc<REGS_EPILOGUE>();
         // ---------------------------------------------------------------- epilogue
-        const int quad = warp & 3;              // TMEM lanes 32*quad .. 32*quad + 31
-        const int half = (warp - EPI_WARP0) >> 2;   // columns 128*half .. 128*half + 127
-        const int r = quad * 32 + lane;         // row within the tile
+        const int quad = warp & 3;                   // TMEM lanes 32*quad .. 32*quad + 31
+        const int half = (warp - EPI_WARP0) >> 2;    // columns 128*half .. 128*half + 127
+        const int r = quad * 32 + lane;              // row within the tile
         const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
         uint32_t j = 0;
         uint64_t acc[64];   // 128 FP32 accumulators as packed pairs (columns 2i, 2i + 1)
 
         for (int t = cluster_id; t < num_tiles; t += num_clusters) {
-            const TileInfo ti = decode_tile<GROUPED, CLUSTER>(t, p, s_tstart, s_off, crank);
-            const int64_t row = ti.row0 + r;
-            const bool row_ok = row >= 0 && row < ti.row_end;
-            const int ncol0 = ti.n0 + half * 128;
-            const bool blk_ok = ncol0 < p.N;
-            const float* sa_ptr = p.a_s + (row_ok ? row : 0);
-            const float* sw_ptr =
-                p.w_s + (static_cast<int64_t>(ti.g) * p.NB + (blk_ok ? ncol0 / 128 : 0)) * KB;
-            // Scales are prefetched two K blocks ahead so that their load latency stays hidden.
-            float sa_c = row_ok ? __ldg(sa_ptr) : 0.0f;
-            float sw_c = blk_ok ? __ldg(sw_ptr) : 0.0f;
-            float sa_n = (row_ok && KB > 1) ? __ldg(sa_ptr + p.rows) : 0.0f;
-            float sw_n = (blk_ok && KB > 1) ? __ldg(sw_ptr + 1) : 0.0f;
-
+            const int ncol0 =
+                decode_tile<GROUPED, CL>(t, p, s_tstart, s_off, static_cast<int>(crank)).n0 +
+                half * 128;
 #pragma unroll
             for (int i = 0; i < 64; i++) acc[i] = 0ull;
 
             bool ok = true;
             for (int kb = 0; kb < KB; kb++, j++) {
-                const float sc = __fmul_rn(sa_c, sw_c);
-                sa_c = sa_n;
-                sw_c = sw_n;
-                if (kb + 2 < KB) {
-                    sa_n = row_ok ? __ldg(sa_ptr + static_cast<int64_t>(kb + 2) * p.rows) : 0.0f;
-                    sw_n = blk_ok ? __ldg(sw_ptr + kb + 2) : 0.0f;
+                // This K block's scales from the scale ring (filled ahead by the loader warp).
+                const uint32_t slot = j % SCALE_SLOTS;
+                const bool sgot =
+                    mbar_wait(sfull0 + 8 * slot, (j / SCALE_SLOTS) & 1u, abort_addr, budget);
+                if (!__all_sync(0xffffffffu, sgot)) {
+                    if (lane == 0) raise_error(p.err, abort_addr, DEV_TIMEOUT_EPILOGUE);
+                    ok = false;
+                    break;
                 }
+                const uint32_t sl = scl0 + slot * SCALE_SLOT_BYTES;
+                const float sc =
+                    __fmul_rn(ld_shared_f32(sl + r * 4), ld_shared_f32(sl + 512 + half * 4));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sempty0 + 8 * slot);
+
                 const uint32_t b = j & 1u;
                 const uint32_t pb = (j >> 1) & 1u;
                 const bool got = mbar_wait(tfull0 + 8 * b, pb, abort_addr, budget);
@@ -395,63 +513,69 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     break;
                 }
                 tc_fence_after();
-                // Eight 16-column chunks; the TMEM load of chunk c+1 is in flight while chunk c
-                // is promoted (two register buffers of 8 packed pairs).
+                // Four 32-column chunks; the TMEM load of chunk c+1 is in flight while chunk c
+                // is promoted (two register buffers of 16 packed pairs).
                 const uint32_t taddr = tmem_base + t_lane + b * BN + half * 128;
                 const uint64_t sc2 = f32x2_splat(sc);
-                uint64_t v0[8], v1[8];
-                tmem_ld_16cols(taddr, v0);
+                uint64_t v0[16], v1[16];
+                tmem_ld_32cols(taddr, v0);
+                tmem_wait_ld(v0);
+                tmem_ld_32cols(taddr + 32, v1);
 #pragma unroll
-                for (int c = 0; c < 8; c += 2) {
-                    tmem_wait_ld(v0);
-                    tmem_ld_16cols(taddr + (c + 1) * 16, v1);
+                for (int i = 0; i < 16; i++) ffma2(acc[i], v0[i], sc2);
+                tmem_wait_ld(v1);
+                tmem_ld_32cols(taddr + 64, v0);
 #pragma unroll
-                    for (int i = 0; i < 8; i++) ffma2(acc[c * 8 + i], v0[i], sc2);
-                    tmem_wait_ld(v1);
-                    if (c + 2 < 8) tmem_ld_16cols(taddr + (c + 2) * 16, v0);
+                for (int i = 0; i < 16; i++) ffma2(acc[16 + i], v1[i], sc2);
+                tmem_wait_ld(v0);
+                tmem_ld_32cols(taddr + 96, v1);
 #pragma unroll
-                    for (int i = 0; i < 8; i++) ffma2(acc[(c + 1) * 8 + i], v1[i], sc2);
-                }
+                for (int i = 0; i < 16; i++) ffma2(acc[32 + i], v0[i], sc2);
+                tmem_wait_ld(v1);
+#pragma unroll
+                for (int i = 0; i < 16; i++) ffma2(acc[48 + i], v1[i], sc2);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(tempty0 + 8 * b);
             }
             if (!ok) break;
 
-            // Store: stage this warp's 32 rows x 128 B at a time in shared memory (16-byte chunk j
-            // of row r at chunk j ^ (r % 8): conflict-free both ways), then write 4 whole rows of
-            // 128 B per warp instruction instead of 32 scattered 16-byte pieces.
+            // Store: stage this warp's 32 rows x 64 B at a time in shared memory, chunk j (16 B)
+            // of row r at position (j + r/2) % 4, which keeps both the row-wise writes and the
+            // column-wise reads free of bank conflicts; then write 8 rows of 64 contiguous bytes
+            // per warp instruction instead of 32 scattered 16-byte pieces.
             {
                 constexpr int ELEM = OUT_F32 ? 4 : 2;
-                constexpr int GCOLS = 128 / ELEM;            // columns per 128-byte staged row
-                const TileInfo ts = decode_tile<GROUPED, CLUSTER>(t, p, s_tstart, s_off, crank);
+                constexpr int GCOLS = 64 / ELEM;             // columns per 64-byte staged row
+                const TileInfo ts =
+                    decode_tile<GROUPED, CL>(t, p, s_tstart, s_off, static_cast<int>(crank));
                 const uint32_t stg = base + L::STG_OFF + (warp - EPI_WARP0) * STG_WARP_BYTES;
                 const int64_t wrow0 = ts.row0 + quad * 32;   // first row of this warp
 #pragma unroll
                 for (int g = 0; g < 128 / GCOLS; g++) {
 #pragma unroll
-                    for (int jc = 0; jc < 8; jc++) {
+                    for (int jc = 0; jc < 4; jc++) {
                         uint4 v;
                         if constexpr (OUT_F32) {
-                            const uint64_t p0 = acc[g * 16 + jc * 2], p1 = acc[g * 16 + jc * 2 + 1];
+                            const uint64_t p0 = acc[g * 8 + jc * 2], p1 = acc[g * 8 + jc * 2 + 1];
                             v = make_uint4(static_cast<uint32_t>(p0), static_cast<uint32_t>(p0 >> 32),
                                            static_cast<uint32_t>(p1), static_cast<uint32_t>(p1 >> 32));
                         } else {
-                            const int q = g * 32 + jc * 4;
+                            const int q = g * 16 + jc * 4;
                             v = make_uint4(pack_bf16x2(f32x2_lo(acc[q]), f32x2_hi(acc[q])),
                                            pack_bf16x2(f32x2_lo(acc[q + 1]), f32x2_hi(acc[q + 1])),
                                            pack_bf16x2(f32x2_lo(acc[q + 2]), f32x2_hi(acc[q + 2])),
                                            pack_bf16x2(f32x2_lo(acc[q + 3]), f32x2_hi(acc[q + 3])));
                         }
-                        st_shared_v4(stg + lane * 128 + ((jc ^ (lane & 7)) * 16), v);
+                        st_shared_v4(stg + lane * 64 + (((jc + (lane >> 1)) & 3) * 16), v);
                     }
                     __syncwarp();
-                    const int ch = lane & 7;
+                    const int ch = lane & 3;
                     const int gcol = ncol0 + g * GCOLS + ch * (16 / ELEM);
 #pragma unroll
-                    for (int i = 0; i < 8; i++) {
-                        const int rr = i * 4 + (lane >> 3);
-                        const uint4 v = ld_shared_v4(stg + rr * 128 + ((ch ^ (rr & 7)) * 16));
+                    for (int i = 0; i < 4; i++) {
+                        const int rr = i * 8 + (lane >> 2);
+                        const uint4 v = ld_shared_v4(stg + rr * 64 + (((ch + (rr >> 1)) & 3) * 16));
                         const int64_t grow = wrow0 + rr;
                         if (grow >= 0 && grow < ts.row_end && gcol < p.N)
                             st_v4(static_cast<uint8_t*>(p.c) + (grow * p.ldc + gcol) * ELEM, v.x, v.y,
@@ -465,31 +589,30 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
 
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync();   // both CTAs are done with TMEM and the peer's barriers
     tc_fence_after();
     if (warp == MMA_WARP) {
         __syncwarp();
-        tmem_dealloc(tmem_base, TMEM_COLS);
+        if constexpr (PAIR) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+        else tmem_dealloc(tmem_base, TMEM_COLS);
     }
-    if constexpr (CLUSTER > 1) cluster_sync();   // no peer still targets this CTA's memory
+    if constexpr (PAIR) cluster_sync();   // no CTA leaves while its peer still deallocates
 }
 
-template <bool GROUPED, bool OUT_F32, int CLUSTER>
+template <bool GROUPED, bool OUT_F32, bool PAIR>
 cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& args,
                        int max_ctas, cudaStream_t stream)
 {
-    auto kern = fp8_blockscaled_gemm_kernel<GROUPED, OUT_F32, CLUSTER>;
+    constexpr int CL = PAIR ? 2 : 1;
+    auto kern = fp8_blockscaled_gemm_kernel<GROUPED, OUT_F32, PAIR>;
     const size_t smem = gemm_smem_bytes(GROUPED, args.G);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    if (CLUSTER > 1) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0);
-        if (e != cudaSuccess) return e;
-    }
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CLUSTER;
+    attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.blockDim = dim3(THREADS);
@@ -498,9 +621,9 @@ cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const GemmA
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     // Persistent grid: as many clusters as fit at once (one CTA per SM), at most one per item.
-    int clusters = max_ctas / CLUSTER;
-    if (CLUSTER > 1) {
-        cfg.gridDim = dim3(static_cast<unsigned>(clusters * CLUSTER));
+    int clusters = max_ctas / CL;
+    if (CL > 1) {
+        cfg.gridDim = dim3(static_cast<unsigned>(clusters * CL));
         int active = 0;
         if (cudaOccupancyMaxActiveClusters(&active, kern, &cfg) != cudaSuccess) {
             cudaGetLastError();   // not fatal: keep one cluster per SM pair
@@ -510,7 +633,7 @@ cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const GemmA
     }
     if (!GROUPED && args.num_tiles < clusters) clusters = args.num_tiles;
     if (clusters < 1) clusters = 1;
-    cfg.gridDim = dim3(static_cast<unsigned>(clusters * CLUSTER));
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * CL));
     e = cudaLaunchKernelEx(&cfg, kern, ma, mb, args);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
@@ -520,8 +643,9 @@ cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const GemmA
 
 size_t gemm_smem_bytes(bool grouped, int G)
 {
-    if (!grouped) return static_cast<size_t>(Layout<false>::GROUP_OFF) + ALIGN_PAD;
-    return static_cast<size_t>(Layout<true>::GROUP_OFF) + ALIGN_PAD +
+    constexpr bool DENSE_PAIR = GEMM_DENSE_CLUSTER == 2;
+    if (!grouped) return static_cast<size_t>(Layout<false, DENSE_PAIR>::GROUP_OFF) + ALIGN_PAD;
+    return static_cast<size_t>(Layout<true, false>::GROUP_OFF) + ALIGN_PAD +
            2 * static_cast<size_t>(G + 1) * sizeof(int);
 }
 
@@ -530,12 +654,12 @@ int gemm_cluster_size(bool grouped) { return grouped ? 1 : GEMM_DENSE_CLUSTER; }
 cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args,
                         bool grouped, bool out_f32, int max_ctas, cudaStream_t stream)
 {
+    constexpr bool DENSE_PAIR = GEMM_DENSE_CLUSTER == 2;
     if (grouped)
-        return out_f32 ? launch_one<true, true, 1>(map_a, map_b, args, max_ctas, stream)
-                       : launch_one<true, false, 1>(map_a, map_b, args, max_ctas, stream);
-    return out_f32
-               ? launch_one<false, true, GEMM_DENSE_CLUSTER>(map_a, map_b, args, max_ctas, stream)
-               : launch_one<false, false, GEMM_DENSE_CLUSTER>(map_a, map_b, args, max_ctas, stream);
+        return out_f32 ? launch_one<true, true, false>(map_a, map_b, args, max_ctas, stream)
+                       : launch_one<true, false, false>(map_a, map_b, args, max_ctas, stream);
+    return out_f32 ? launch_one<false, true, DENSE_PAIR>(map_a, map_b, args, max_ctas, stream)
+                   : launch_one<false, false, DENSE_PAIR>(map_a, map_b, args, max_ctas, stream);
 }
 
 }  // namespace fp8bs

@@ -27,6 +27,7 @@ enum DeviceError : int {
     DEV_TIMEOUT_MMA_FULL = 3,   // MMA issuer: a smem stage never filled
     DEV_TIMEOUT_EPILOGUE = 4,   // epilogue: a K-block partial never arrived
     DEV_TIMEOUT_DRAIN = 5,      // clean-up: in-flight copies or MMAs did not finish
+    DEV_TIMEOUT_SCALES = 6,     // scale loader: a scale slot never became free
 };
 
 struct GemmArgs {
