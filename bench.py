@@ -247,7 +247,11 @@ def run_ours(args, rank, world, local_rank):
            "ms_per_step": round(e2e_ms, 4)}
 
     peaks, peak_src = load_peaks()
-    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+    # The GEMM is timed inside a seconds-long run of back-to-back steps (power-capped clocks), so
+    # its roofline uses the sustained BF16 figure x the nominal FP8/BF16 ratio; the fraction of
+    # the burst figure is reported next to it.
+    fp8_peak = peaks["bf16_tflops_sustained"] * FP8_OVER_BF16
+    fp8_peak_burst = peaks["bf16_tflops"] * FP8_OVER_BF16
     g_tflops = gemm_flops(M, N, K) / (g_ms * 1e-3) / 1e12
     qa_gbs = M * K * ACT_BYTES_PER_ELEM / (qa_ms * 1e-3) / 1e9
     qw_gbs = N * K * W_BYTES_PER_ELEM / (qw_ms * 1e-3) / 1e9
@@ -276,8 +280,11 @@ def run_ours(args, rank, world, local_rank):
                      "achieved": round(g_tflops, 1), "peak": round(fp8_peak, 1),
                      "unit": "TFLOP/s", "frac": round(g_tflops / fp8_peak, 4),
                      "traffic": traffic,
-                     "peak_source": f"{peak_src}: 2 x bf16 burst {peaks['bf16_tflops']} TFLOP/s "
-                                    "(nominal fp8/bf16 ratio 4.5/2.25)"},
+                     "peak_source": f"{peak_src}: 2 x bf16 sustained "
+                                    f"{peaks['bf16_tflops_sustained']} TFLOP/s (nominal fp8/bf16 "
+                                    "ratio 4.5/2.25); kernel timed inside a long step",
+                     "frac_of_burst_peak": round(g_tflops / fp8_peak_burst, 4),
+                     "burst_peak": round(fp8_peak_burst, 1)},
         "kernels": {
             "quant_act_1x128": {"ms": round(qa_ms, 5), "GB/s": round(qa_gbs, 1),
                                 "frac_hbm": round(qa_gbs / peaks["hbm_gbs"], 4)},
@@ -294,7 +301,7 @@ def run_ours(args, rank, world, local_rank):
     if not args.no_extras:
         del a, w, aq, a_s, wq, w_s, c, a_h, w_h, c_h
         torch.cuda.empty_cache()
-        line["workloads"] = run_extras(F, dev, peaks, fp8_peak)
+        line["workloads"] = run_extras(F, dev, peaks, fp8_peak_burst)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget_s)
     return line
