@@ -19,6 +19,7 @@ namespace fp8bs {
 namespace host {
 
 std::mutex g_mu;
+int g_fault_skip_release = -1;
 DeviceInfo g_dev[MAX_DEVICES];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -139,6 +140,15 @@ int check_gemm_args(const void* a_q, const void* a_s, const void* w_q, const voi
 }
 
 }  // namespace host
+
+int take_fault_skip_release()
+{
+    std::lock_guard<std::mutex> lock(host::g_mu);
+    const int v = host::g_fault_skip_release;
+    host::g_fault_skip_release = -1;
+    return v;
+}
+
 }  // namespace fp8bs
 
 extern "C" {
@@ -201,6 +211,7 @@ int fp8_blockscaled_gemm(const uint8_t* a_q, const float* a_s, const uint8_t* w_
     args.G = 1;
     args.err = d->err;
     args.budget = wait_budget();
+    args.fault_skip_release = -1;
     return cuda_status(launch_gemm(ma, mb, args, false, out_dtype == FP8BS_OUT_F32, d->num_sms,
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -241,6 +252,7 @@ int fp8_blockscaled_grouped_gemm(const uint8_t* a_q, const float* a_s, const uin
     args.G = static_cast<int>(G);
     args.err = d->err;
     args.budget = wait_budget();
+    args.fault_skip_release = take_fault_skip_release();
     // At most ceil(R/128) + G m-tiles exist across the groups; the exact count is formed on the
     // device from the offsets, and CTAs without a tile exit at once.
     const int64_t bound = ((R + GEMM_BM - 1) / GEMM_BM + G) * args.NT;
@@ -248,6 +260,14 @@ int fp8_blockscaled_grouped_gemm(const uint8_t* a_q, const float* a_s, const uin
     const int max_ctas = static_cast<int>(bound < d->num_sms ? bound : d->num_sms);
     return cuda_status(launch_gemm(ma, mb, args, true, out_dtype == FP8BS_OUT_F32, max_ctas,
                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fp8bs_debug_skip_release(int at)
+{
+    if (at < 0) return FP8BS_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_fault_skip_release = at;
+    return FP8BS_OK;
 }
 
 const char* fp8bs_status_string(int status)

@@ -338,9 +338,9 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                         }
                     }
                 }
-                if (!ok && leader) {
-                    // The MMA side may never consume what is in flight: wait for the last copy
-                    // issued into every stage before the CTA may exit.
+                if ((!ok || ld_shared_volatile_u32(abort_addr) != 0) && leader) {
+                    // After an abort the MMA side may never consume what is in flight: wait for
+                    // the last copy issued into every stage before the CTA may exit.
                     const uint32_t first = it > STAGES ? it - STAGES : 0;
                     for (uint32_t i = first; i < it; i++)
                         if (!mbar_wait(full0 + 8 * (i % STAGES), (i / STAGES) & 1u, 0u, budget))
@@ -536,7 +536,9 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                 for (int i = 0; i < 16; i++) ffma2(acc[48 + i], v1[i], sc2);
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(tempty0 + 8 * b);
+                // (test hook: one epilogue warp can be told to skip one release, see GemmArgs)
+                if (lane == 0 && !(warp == EPI_WARP0 && static_cast<int>(j) == p.fault_skip_release))
+                    mbar_arrive(tempty0 + 8 * b);
             }
             if (!ok) break;
 

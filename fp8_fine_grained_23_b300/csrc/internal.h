@@ -46,6 +46,8 @@ struct GemmArgs {
     int G;
     int* err;                 // device error word
     long long budget;         // spin-wait budget in SM clock cycles
+    int fault_skip_release;   // test hook: accumulation index at which one epilogue warp skips
+                              // its TMEM release (-1: never); set by fp8bs_debug_skip_release
 };
 
 cudaError_t launch_quant_act(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
@@ -54,6 +56,10 @@ cudaError_t launch_quant_act(const void* x, int64_t M, int64_t K, int64_t ldx, u
 cudaError_t launch_quant_weight(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
                                 int64_t ldq, float* scales, cudaStream_t stream);
 // max_ctas: the persistent grid's upper bound (the SM count); the launcher sizes the grid.
+// One-shot test hook (api.cu): the index for GemmArgs::fault_skip_release of the next grouped
+// GEMM launch, then back to -1.
+int take_fault_skip_release();
+
 cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args,
                         bool grouped, bool out_f32, int max_ctas, cudaStream_t stream);
 int gemm_cluster_size(bool grouped);

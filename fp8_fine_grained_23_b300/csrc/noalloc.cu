@@ -96,6 +96,7 @@ extern "C" int fp8_blockscaled_gemm_noalloc(const uint8_t* a_q, const float* a_s
     args.G = 1;
     args.err = scratch;   // the error word must start at zero on every call
     args.budget = wait_budget();
+    args.fault_skip_release = -1;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(scratch, 0, NOALLOC_WORDS_PER_CALL * sizeof(int), s) != cudaSuccess) {
         cudaGetLastError();

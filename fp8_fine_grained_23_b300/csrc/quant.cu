@@ -235,8 +235,8 @@ quant_act_1x128_kernel(const QuantActArgs p)
                 bulk_load(base + slot * SEG_BYTES, p.x + row * p.ldx + static_cast<int64_t>(tile0) * 128,
                           bytes, bar_full + 8 * slot);
             }
-            if (!ok) {
-                // wait for the copies already issued before the CTA exits
+            if (!ok || ld_shared_volatile_u32(abort_addr) != 0) {
+                // after an abort, wait for the copies already issued before the CTA exits
                 for (int64_t j = (i > QA_SLOTS ? i - QA_SLOTS : 0); j < i; j++)
                     if (!mbar_wait(bar_full + 8 * qa_slot(j), qa_phase(j), 0u, p.budget))
                         atomicCAS(p.err, 0, DEV_TIMEOUT_DRAIN);

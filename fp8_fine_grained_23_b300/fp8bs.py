@@ -32,9 +32,10 @@ lib.fp8_blockscaled_grouped_gemm.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i6
 lib.fp8bs_status_string.argtypes = [_int]
 lib.fp8bs_status_string.restype = ctypes.c_char_p
 lib.fp8bs_last_error.argtypes = [_p]
+lib.fp8bs_debug_skip_release.argtypes = [_int]
 for _f in (lib.fp8_quant_act_1x128, lib.fp8_quant_weight_128x128, lib.fp8_blockscaled_gemm,
            lib.fp8_blockscaled_gemm_noalloc, lib.fp8_blockscaled_grouped_gemm,
-           lib.fp8bs_last_error):
+           lib.fp8bs_last_error, lib.fp8bs_debug_skip_release):
     _f.restype = _int
 
 FP8BS_OK = 0

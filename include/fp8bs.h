@@ -158,6 +158,17 @@ int fp8_blockscaled_gemm_noalloc(const uint8_t *a_q, const float *a_s,
                                  int64_t M, int64_t N, int64_t K,
                                  void *c, int64_t ldc, int out_dtype, fp8bs_stream_t stream);
 
+/*
+ * Test hook for failure detection (not for production use): the next grouped GEMM launch
+ * (fp8_blockscaled_grouped_gemm) runs with one epilogue warp skipping its release of the TMEM
+ * accumulator at accumulation step `at` (0-based over the CTA's K blocks). A release that never
+ * comes makes the MMA issuer's wait run past its budget; the kernel then records
+ * FP8BS_ERR_TIMEOUT, every role stops and drains its in-flight copies and MMAs, and the kernel
+ * returns, so the CUDA context stays usable. One-shot: later launches are unaffected.
+ * Returns FP8BS_ERR_INVALID_ARG for at < 0.
+ */
+int fp8bs_debug_skip_release(int at);
+
 /* Human-readable name of a status code. The string is static. */
 const char *fp8bs_status_string(int status);
 

@@ -92,6 +92,10 @@ def test_grouped_gemm_argument_checks(F):
     assert g(P16, P4, P16, P4, P4, 2, 0, 32, 128, P16, 32, 0, None) == 0       # R == 0
 
 
+def test_debug_hook_rejects_negative_index(F):
+    assert F.lib.fp8bs_debug_skip_release(-1) == F.FP8BS_ERR_INVALID_ARG
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU behaviour")
 def test_valid_call_without_gpu_fails_loudly(F):
     st = F.lib.fp8_quant_act_1x128(P16, 4, 128, 128, P16, 128, P4, None)
