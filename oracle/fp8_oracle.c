@@ -36,6 +36,14 @@
  *  - Scale layouts: activation scales [K/128][M] (M contiguous); weight scales
  *    [ceil(N/128)][K/128] (K blocks contiguous). A last, partial weight block's amax covers
  *    only its real rows.
+ *  - Backward pass ([codingmall] "Định dạng E4M3 hợp nhất", [dtcms] 三.2: the same E4M3
+ *    format for the backward pass). The pages name no backward tile shapes. A block-scaled
+ *    contraction needs one scale per 128-long block of the contracted index, so:
+ *      dgrad dX = dY W    contracts over N: dY in 1x128 tiles (the forward quantizer), W in
+ *                         its 128x128 blocks, its codes laid out as W^T [K][N];
+ *      wgrad dW = dY^T X  contracts over the M tokens: dY and X in 128x1 tiles (128 tokens of
+ *                         one channel), codes laid out transposed [channels][M], and the GEMM
+ *                         takes a per-row scale on both operands ("1d1d").
  */
 #include <math.h>
 #include <stdint.h>
@@ -200,6 +208,54 @@ void orc_quant_weight_128x128(const uint16_t *w, int64_t N, int64_t K, int64_t l
     }
 }
 
+/* 128x1 activation tiles for the weight-gradient GEMM: one scale per 128 consecutive rows
+ * (tokens) of one column (channel). x: BF16 bits [M][ldx]; the codes are written transposed,
+ * qt[k][m] at qt + k*ldqt + m (so the tokens become the contiguous, contracted index); scales
+ * s[mb][k] at s + mb*K + k. M must be a multiple of 128. */
+void orc_quant_act_128x1(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                         uint8_t *qt, int64_t ldqt, float *s)
+{
+    int64_t MB = M / 128;
+    for (int64_t k = 0; k < K; k++) {
+        for (int64_t mb = 0; mb < MB; mb++) {
+            float amax = 0.0f;
+            tile_scale_t t;
+            for (int i = 0; i < 128; i++)
+                amax = fmaxf(amax, fabsf(bf16_bits_to_float(x[(mb * 128 + i) * ldx + k])));
+            t = tile_scale(amax);
+            for (int i = 0; i < 128; i++)
+                qt[k * ldqt + mb * 128 + i] =
+                    tile_encode(bf16_bits_to_float(x[(mb * 128 + i) * ldx + k]), &t);
+            s[mb * K + k] = t.s;
+        }
+    }
+}
+
+/* 128x128 weight blocks with the codes written transposed, for the data-gradient GEMM that
+ * contracts over N: qt[k][n] at qt + k*ldqt + n, scales st[kb][nb] at st + kb*(N/128) + nb.
+ * The blocks, their amax and their codes are those of the forward weight quantizer.
+ * N and K must be multiples of 128. */
+void orc_quant_weight_128x128_t(const uint16_t *w, int64_t N, int64_t K, int64_t ldw,
+                                uint8_t *qt, int64_t ldqt, float *st)
+{
+    int64_t KB = K / 128;
+    int64_t NB = N / 128;
+    for (int64_t nb = 0; nb < NB; nb++) {
+        for (int64_t kb = 0; kb < KB; kb++) {
+            float amax = 0.0f;
+            tile_scale_t t;
+            for (int64_t n = nb * 128; n < nb * 128 + 128; n++)
+                for (int64_t k = kb * 128; k < kb * 128 + 128; k++)
+                    amax = fmaxf(amax, fabsf(bf16_bits_to_float(w[n * ldw + k])));
+            t = tile_scale(amax);
+            for (int64_t n = nb * 128; n < nb * 128 + 128; n++)
+                for (int64_t k = kb * 128; k < kb * 128 + 128; k++)
+                    qt[k * ldqt + n] = tile_encode(bf16_bits_to_float(w[n * ldw + k]), &t);
+            st[kb * NB + nb] = t.s;
+        }
+    }
+}
+
 /* ------------------------------------------------------------------------------------ */
 /* Block-scaled GEMM: C = A * W^T on the quantized operands                               */
 /*   C[m,n] = sum_kb s_a[kb][m] * s_w[n/128][kb] * sum_{k in kb} dec(a[m,k]) * dec(w[n,k])  */
@@ -218,13 +274,13 @@ static void dec_table(double dec[256])
  * *abs_out gets sum_k |a_hat_k * w_hat_k| (dequantized operands), the error-bound weight. */
 static double point_f64(const double *dec,
                         const uint8_t *arow, const float *as, int64_t as_ld, int64_t m,
-                        const uint8_t *wrow, const float *ws_row, int64_t KB,
+                        const uint8_t *wrow, const float *ws_row, int64_t ws_step, int64_t KB,
                         double *abs_out)
 {
     double c = 0.0, cabs = 0.0;
     for (int64_t kb = 0; kb < KB; kb++) {
         double part = 0.0, part_abs = 0.0;
-        double sc = (double)as[kb * as_ld + m] * (double)ws_row[kb];
+        double sc = (double)as[kb * as_ld + m] * (double)ws_row[kb * ws_step];
         for (int k = 0; k < 128; k++) {
             double p = dec[arow[kb * 128 + k]] * dec[wrow[kb * 128 + k]];
             part += p;
@@ -239,14 +295,16 @@ static double point_f64(const double *dec,
 }
 
 /* The same element with an FP32 partial per K block (sequential, products exact in FP32)
- * and an FP32 fused multiply-add promotion: acc = fma(partial, s_a * s_w, acc). */
+ * and an FP32 fused multiply-add promotion: acc = fma(partial, s_a * s_w, acc).
+ * ws_row[kb * ws_step] is the second operand's scale of K block kb (step 1 for a weight
+ * block row, N for per-row scales [K/128][N]). */
 static float point_f32(const double *dec, const uint8_t *arow, const float *as, int64_t as_ld, int64_t m,
-                       const uint8_t *wrow, const float *ws_row, int64_t KB)
+                       const uint8_t *wrow, const float *ws_row, int64_t ws_step, int64_t KB)
 {
     float acc = 0.0f;
     for (int64_t kb = 0; kb < KB; kb++) {
         float part = 0.0f;
-        float sc = as[kb * as_ld + m] * ws_row[kb];
+        float sc = as[kb * as_ld + m] * ws_row[kb * ws_step];
         for (int k = 0; k < 128; k++)
             part += (float)dec[arow[kb * 128 + k]] * (float)dec[wrow[kb * 128 + k]];
         acc = fmaf(part, sc, acc);
@@ -273,13 +331,13 @@ void orc_gemm_points(const uint8_t *aq, int64_t lda, const float *as,
         const uint8_t *wrow = wq + n * ldw;
         const float *ws_row = ws + (n / 128) * KB;
         double cabs;
-        double c = point_f64(dec, arow, as, M, m, wrow, ws_row, KB, &cabs);
+        double c = point_f64(dec, arow, as, M, m, wrow, ws_row, 1, KB, &cabs);
         if (out_f64)
             out_f64[i] = c;
         if (out_abs)
             out_abs[i] = cabs;
         if (out_f32)
-            out_f32[i] = point_f32(dec, arow, as, M, m, wrow, ws_row, KB);
+            out_f32[i] = point_f32(dec, arow, as, M, m, wrow, ws_row, 1, KB);
     }
 }
 
@@ -295,12 +353,38 @@ void orc_gemm_f64(const uint8_t *aq, int64_t lda, const float *as,
         for (int64_t n = 0; n < N; n++) {
             double ab;
             double v = point_f64(dec, aq + m * lda, as, M, m, wq + n * ldw, ws + (n / 128) * KB,
-                                 KB, &ab);
+                                 1, KB, &ab);
             if (c)
                 c[m * N + n] = v;
             if (cabs)
                 cabs[m * N + n] = ab;
         }
+}
+
+/* GEMM with a per-row scale on both operands ("1d1d", the weight-gradient GEMM):
+ *   C[m,n] = sum_kb s_a[kb][m] * s_b[kb][n] * sum_{k in kb} dec(a[m,k]) * dec(b[n,k]).
+ * aq [M][lda], as [K/128][M]; bq [N][ldb], bs [K/128][N]. Selected elements (pm[i], pn[i]);
+ * out_f64 / out_abs / out_f32 may each be NULL. */
+void orc_gemm_1d1d_points(const uint8_t *aq, int64_t lda, const float *as,
+                          const uint8_t *bq, int64_t ldb, const float *bs,
+                          int64_t M, int64_t N, int64_t K,
+                          int64_t npts, const int64_t *pm, const int64_t *pn,
+                          double *out_f64, double *out_abs, float *out_f32)
+{
+    int64_t KB = K / 128;
+    double dec[256];
+    dec_table(dec);
+    for (int64_t i = 0; i < npts; i++) {
+        int64_t m = pm[i], n = pn[i];
+        double cabs;
+        double c = point_f64(dec, aq + m * lda, as, M, m, bq + n * ldb, bs + n, N, KB, &cabs);
+        if (out_f64)
+            out_f64[i] = c;
+        if (out_abs)
+            out_abs[i] = cabs;
+        if (out_f32)
+            out_f32[i] = point_f32(dec, aq + m * lda, as, M, m, bq + n * ldb, bs + n, N, KB);
+    }
 }
 
 /* Grouped GEMM for routed experts: row r belongs to expert e with off[e] <= r < off[e+1]
@@ -331,7 +415,7 @@ void orc_grouped_gemm_points(const uint8_t *aq, int64_t lda, const float *as,
             continue;
         }
         c = point_f64(dec, aq + r * lda, as, R, r,
-                      wq + (e * N + n) * ldw, ws + (e * NB + n / 128) * KB, KB, &cabs);
+                      wq + (e * N + n) * ldw, ws + (e * NB + n / 128) * KB, 1, KB, &cabs);
         if (out_f64)
             out_f64[i] = c;
         if (out_abs)

@@ -63,9 +63,15 @@ def lib() -> ctypes.CDLL:
             L.orc_grouped_gemm_points.argtypes = [_p, _i64, _p, _p, _i64, _p, _p, _i64, _i64,
                                                   _i64, _i64, _i64, _p, _p, _p, _p]
             L.orc_gemm_unquantized_f64.argtypes = [_p, _i64, _p, _i64, _i64, _i64, _i64, _p]
+            L.orc_quant_act_128x1.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p]
+            L.orc_quant_weight_128x128_t.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p]
+            L.orc_gemm_1d1d_points.argtypes = [_p, _i64, _p, _p, _i64, _p, _i64, _i64, _i64,
+                                               _i64, _p, _p, _p, _p, _p]
             for f in (L.orc_e4m3_encode_array, L.orc_e4m3_decode_array, L.orc_quant_act_1x128,
                       L.orc_quant_weight_128x128, L.orc_gemm_points, L.orc_gemm_f64,
-                      L.orc_grouped_gemm_points, L.orc_gemm_unquantized_f64):
+                      L.orc_grouped_gemm_points, L.orc_gemm_unquantized_f64,
+                      L.orc_quant_act_128x1, L.orc_quant_weight_128x128_t,
+                      L.orc_gemm_1d1d_points):
                 f.restype = None
             _lib = L
         return _lib
@@ -126,6 +132,30 @@ def quant_weight_128x128(w_bits) -> tuple[np.ndarray, np.ndarray]:
     return q, s
 
 
+def quant_act_128x1(x_bits) -> tuple[np.ndarray, np.ndarray]:
+    """Backward (weight-gradient) tiles of 128 rows x 1 column. x_bits: uint16 BF16 bits
+    [M][K], M % 128 == 0. Returns (codes uint8 [K][M], transposed; scales f32 [M/128][K])."""
+    x = _c(x_bits, np.uint16)
+    M, K = x.shape
+    assert M % 128 == 0
+    qt = np.empty((K, M), np.uint8)
+    s = np.empty((M // 128, K), np.float32)
+    lib().orc_quant_act_128x1(_ptr(x), M, K, K, _ptr(qt), M, _ptr(s))
+    return qt, s
+
+
+def quant_weight_128x128_t(w_bits) -> tuple[np.ndarray, np.ndarray]:
+    """128x128 blocks of w [N][K] (N, K % 128 == 0) with the codes written as W^T. Returns
+    (codes uint8 [K][N], scales f32 [K/128][N/128])."""
+    w = _c(w_bits, np.uint16)
+    N, K = w.shape
+    assert N % 128 == 0 and K % 128 == 0
+    qt = np.empty((K, N), np.uint8)
+    st = np.empty((K // 128, N // 128), np.float32)
+    lib().orc_quant_weight_128x128_t(_ptr(w), N, K, K, _ptr(qt), N, _ptr(st))
+    return qt, st
+
+
 # --------------------------------------------------------------------------------------
 # GEMMs
 # --------------------------------------------------------------------------------------
@@ -157,6 +187,32 @@ def gemm_points(aq, a_s, wq, w_s, pm, pn, want_f32: bool = False):
     lib().orc_gemm_points(_ptr(aq), K, _ptr(a_s), _ptr(wq), K, _ptr(w_s), M, N, K,
                           n, _ptr(pm), _ptr(pn), _ptr(c), _ptr(cabs), _ptr(c32))
     return (c, cabs, c32) if want_f32 else (c, cabs)
+
+
+def gemm_1d1d_points(aq, a_s, bq, b_s, pm, pn, want_f32: bool = False):
+    """Per-row scales on both operands: aq [M][K], a_s [K/128][M]; bq [N][K], b_s [K/128][N].
+    Returns (c64, cabs) or (c64, cabs, c32) at (pm[i], pn[i])."""
+    aq, bq = _c(aq, np.uint8), _c(bq, np.uint8)
+    a_s, b_s = _c(a_s, np.float32), _c(b_s, np.float32)
+    pm, pn = _c(pm, np.int64), _c(pn, np.int64)
+    M, K = aq.shape
+    N = bq.shape[0]
+    assert a_s.shape == (K // 128, M) and b_s.shape == (K // 128, N)
+    n = pm.size
+    c = np.empty(n, np.float64)
+    cabs = np.empty(n, np.float64)
+    c32 = np.empty(n, np.float32) if want_f32 else None
+    lib().orc_gemm_1d1d_points(_ptr(aq), K, _ptr(a_s), _ptr(bq), K, _ptr(b_s), M, N, K,
+                               n, _ptr(pm), _ptr(pn), _ptr(c), _ptr(cabs), _ptr(c32))
+    return (c, cabs, c32) if want_f32 else (c, cabs)
+
+
+def gemm_1d1d_f64(aq, a_s, bq, b_s) -> tuple[np.ndarray, np.ndarray]:
+    """Whole output of gemm_1d1d_points, (C64 [M][N], Cabs [M][N])."""
+    M, N = aq.shape[0], bq.shape[0]
+    mm, nn = np.meshgrid(np.arange(M), np.arange(N), indexing="ij")
+    c, cabs = gemm_1d1d_points(aq, a_s, bq, b_s, mm.ravel(), nn.ravel())
+    return c.reshape(M, N), cabs.reshape(M, N)
 
 
 def grouped_gemm_points(aq, a_s, wq, w_s, offsets, pr, pn):
