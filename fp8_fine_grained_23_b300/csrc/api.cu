@@ -139,6 +139,63 @@ int check_gemm_args(const void* a_q, const void* a_s, const void* w_q, const voi
     return FP8BS_OK;
 }
 
+// Transposing quantizers: the rows are the contracted index of the later GEMM, in blocks of
+// 128 (rows % 128 == 0); codes [K][ldqt >= rows].
+int check_transpose_quant_args(const void* in, int64_t rows, int64_t K, int64_t ld_in,
+                               const void* qt, int64_t ldqt, const void* scales)
+{
+    if (rows < 0 || rows % 128 != 0 || K <= 0 || K % 128 != 0 || ld_in < K || ldqt < rows)
+        return FP8BS_ERR_INVALID_ARG;
+    if (rows > INT32_MAX || K > INT32_MAX || rows / 128 > 65535) return FP8BS_ERR_INVALID_ARG;
+    if (rows == 0) return FP8BS_OK;
+    if (!in || !qt || !scales) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned16(in) || !aligned16(qt) || !aligned4(scales) || ld_in % 8 != 0 ||
+        ldqt % 16 != 0)
+        return FP8BS_ERR_MISALIGNED;
+    return FP8BS_OK;
+}
+
+// Dense GEMM launch shared by fp8_blockscaled_gemm (block-scaled W) and
+// fp8_blockscaled_gemm_1d1d (per-row B scales): the same tiles, maps and persistent grid.
+int dense_gemm(GemmKind kind, const uint8_t* a_q, const float* a_s, const uint8_t* w_q,
+               const float* w_s, int64_t M, int64_t N, int64_t K, void* c, int64_t ldc,
+               int out_dtype, fp8bs_stream_t stream)
+{
+    int st = check_gemm_args(a_q, a_s, w_q, w_s, M, N, K, c, ldc, out_dtype);
+    if (st != FP8BS_OK || M == 0) return st;
+    DeviceInfo* d = nullptr;
+    if ((st = current_device(&d)) != FP8BS_OK) return st;
+    if ((st = ensure_error_word(d)) != FP8BS_OK) return st;
+    if ((st = ensure_encoder()) != FP8BS_OK) return st;
+
+    const int cluster = gemm_cluster_size(false);
+    CUtensorMap ma, mb;
+    if ((st = make_code_map(&ma, a_q, K, M, K, GEMM_BM)) != FP8BS_OK) return st;
+    if ((st = make_code_map(&mb, w_q, K, N, K, GEMM_BN / cluster)) != FP8BS_OK) return st;
+
+    GemmArgs args{};
+    args.a_s = a_s;
+    args.w_s = w_s;
+    args.c = c;
+    args.ldc = ldc;
+    args.rows = M;
+    args.N = static_cast<int>(N);
+    args.KB = static_cast<int>(K / 128);
+    args.NB = static_cast<int>((N + 127) / 128);
+    args.NT = static_cast<int>((N + GEMM_BN - 1) / GEMM_BN);
+    args.MT = static_cast<int>((M + GEMM_BM - 1) / GEMM_BM);
+    const int64_t items = static_cast<int64_t>((args.MT + cluster - 1) / cluster) * args.NT;
+    if (items > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
+    args.num_tiles = static_cast<int>(items);
+    args.offsets = nullptr;
+    args.G = 1;
+    args.err = d->err;
+    args.budget = wait_budget();
+    args.fault_skip_release = -1;
+    return cuda_status(launch_gemm(ma, mb, args, kind, out_dtype == FP8BS_OUT_F32, d->num_sms,
+                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace host
 
 int take_fault_skip_release()
@@ -181,39 +238,38 @@ int fp8_blockscaled_gemm(const uint8_t* a_q, const float* a_s, const uint8_t* w_
                          const float* w_s, int64_t M, int64_t N, int64_t K, void* c, int64_t ldc,
                          int out_dtype, fp8bs_stream_t stream)
 {
-    int st = check_gemm_args(a_q, a_s, w_q, w_s, M, N, K, c, ldc, out_dtype);
+    return fp8bs::host::dense_gemm(GemmKind::DENSE, a_q, a_s, w_q, w_s, M, N, K, c, ldc,
+                                   out_dtype, stream);
+}
+
+int fp8_blockscaled_gemm_1d1d(const uint8_t* a_q, const float* a_s, const uint8_t* b_q,
+                              const float* b_s, int64_t M, int64_t N, int64_t K, void* c,
+                              int64_t ldc, int out_dtype, fp8bs_stream_t stream)
+{
+    return fp8bs::host::dense_gemm(GemmKind::ROW_SCALED, a_q, a_s, b_q, b_s, M, N, K, c, ldc,
+                                   out_dtype, stream);
+}
+
+int fp8_quant_act_128x1(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* qt,
+                        int64_t ldqt, float* scales, fp8bs_stream_t stream)
+{
+    int st = check_transpose_quant_args(x, M, K, ldx, qt, ldqt, scales);
     if (st != FP8BS_OK || M == 0) return st;
     DeviceInfo* d = nullptr;
     if ((st = current_device(&d)) != FP8BS_OK) return st;
-    if ((st = ensure_error_word(d)) != FP8BS_OK) return st;
-    if ((st = ensure_encoder()) != FP8BS_OK) return st;
+    return cuda_status(launch_quant_act_128x1(x, M, K, ldx, qt, ldqt, scales,
+                                              reinterpret_cast<cudaStream_t>(stream)));
+}
 
-    const int cluster = gemm_cluster_size(false);
-    CUtensorMap ma, mb;
-    if ((st = make_code_map(&ma, a_q, K, M, K, GEMM_BM)) != FP8BS_OK) return st;
-    if ((st = make_code_map(&mb, w_q, K, N, K, GEMM_BN / cluster)) != FP8BS_OK) return st;
-
-    GemmArgs args{};
-    args.a_s = a_s;
-    args.w_s = w_s;
-    args.c = c;
-    args.ldc = ldc;
-    args.rows = M;
-    args.N = static_cast<int>(N);
-    args.KB = static_cast<int>(K / 128);
-    args.NB = static_cast<int>((N + 127) / 128);
-    args.NT = static_cast<int>((N + GEMM_BN - 1) / GEMM_BN);
-    args.MT = static_cast<int>((M + GEMM_BM - 1) / GEMM_BM);
-    const int64_t items = static_cast<int64_t>((args.MT + cluster - 1) / cluster) * args.NT;
-    if (items > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
-    args.num_tiles = static_cast<int>(items);
-    args.offsets = nullptr;
-    args.G = 1;
-    args.err = d->err;
-    args.budget = wait_budget();
-    args.fault_skip_release = -1;
-    return cuda_status(launch_gemm(ma, mb, args, false, out_dtype == FP8BS_OUT_F32, d->num_sms,
-                                   reinterpret_cast<cudaStream_t>(stream)));
+int fp8_quant_weight_128x128_t(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* qt,
+                               int64_t ldqt, float* scales_t, fp8bs_stream_t stream)
+{
+    int st = check_transpose_quant_args(w, N, K, ldw, qt, ldqt, scales_t);
+    if (st != FP8BS_OK || N == 0) return st;
+    DeviceInfo* d = nullptr;
+    if ((st = current_device(&d)) != FP8BS_OK) return st;
+    return cuda_status(launch_quant_weight_t(w, N, K, ldw, qt, ldqt, scales_t,
+                                             reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int fp8_blockscaled_grouped_gemm(const uint8_t* a_q, const float* a_s, const uint8_t* w_q,
@@ -258,7 +314,7 @@ int fp8_blockscaled_grouped_gemm(const uint8_t* a_q, const float* a_s, const uin
     const int64_t bound = ((R + GEMM_BM - 1) / GEMM_BM + G) * args.NT;
     if (bound > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
     const int max_ctas = static_cast<int>(bound < d->num_sms ? bound : d->num_sms);
-    return cuda_status(launch_gemm(ma, mb, args, true, out_dtype == FP8BS_OUT_F32, max_ctas,
+    return cuda_status(launch_gemm(ma, mb, args, GemmKind::GROUPED, out_dtype == FP8BS_OUT_F32, max_ctas,
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 

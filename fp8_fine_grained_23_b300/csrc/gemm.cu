@@ -72,21 +72,24 @@ constexpr int B_BYTES = BN * BK;           // the whole W tile
 constexpr int STG_WARP_BYTES = 32 * 64;    // output staging per epilogue warp: 32 rows x 64 B
 constexpr int STG_BYTES = NUM_EPI_WARPS * STG_WARP_BYTES;
 constexpr int SCALE_SLOTS = 8;             // scale ring: one slot per K block in flight
-constexpr int SCALE_SLOT_BYTES = 528;      // 128 activation scales + 2 weight scales, padded
+constexpr int SCALE_SLOT_BYTES_BLOCK = 528;   // 128 activation scales + 2 weight-block scales
+constexpr int SCALE_SLOT_BYTES_ROWS = 1536;   // 128 A-row scales + 256 B-row scales
 constexpr int ALIGN_PAD = 1024;            // 128-byte-swizzled tiles need 1024-byte alignment
 
 // Shared-memory layout per CTA. PAIR: a CTA holds its A tile and half of the W tile.
-template <bool GROUPED, bool PAIR>
+// RS: the B operand has a scale per row and K block (the 1d1d GEMM) instead of per 128x128 block.
+template <bool GROUPED, bool PAIR, bool RS>
 struct Layout {
+    static constexpr int SLOT = RS ? SCALE_SLOT_BYTES_ROWS : SCALE_SLOT_BYTES_BLOCK;
     static constexpr int CL = PAIR ? 2 : 1;              // CTAs per cluster
     static constexpr int B_PART = B_BYTES / CL;          // W rows held by this CTA
     static constexpr int STAGE = A_BYTES + B_PART;
-    static constexpr int STAGES = PAIR ? 6 : (GROUPED ? 3 : 4);
+    static constexpr int STAGES = PAIR ? 6 : 4;
     static constexpr int A_OFF = 0;
     static constexpr int B_OFF = STAGES * A_BYTES;
     static constexpr int STG_OFF = STAGES * STAGE;
     static constexpr int SCL_OFF = STG_OFF + STG_BYTES;
-    static constexpr int BAR_OFF = SCL_OFF + SCALE_SLOTS * SCALE_SLOT_BYTES;
+    static constexpr int BAR_OFF = SCL_OFF + SCALE_SLOTS * SLOT;
     // full[S], empty[S], tfull[2], tempty[2], drain, sfull[SCALE_SLOTS], sempty[SCALE_SLOTS]
     static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * SCALE_SLOTS;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
@@ -168,6 +171,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
     return r;
 }
 
+__device__ __forceinline__ uint64_t ld_shared_u64(uint32_t addr)
+{
+    uint64_t v;
+    asm volatile("ld.shared.b64 %0, [%1];" : "=l"(v) : "r"(addr));
+    return v;
+}
+
 __device__ __forceinline__ float ld_shared_f32(uint32_t addr)
 {
     float v;
@@ -199,12 +209,12 @@ __device__ __forceinline__ void st_v4(void* p, uint32_t a, uint32_t b, uint32_t 
                  : "memory");
 }
 
-template <bool GROUPED, bool OUT_F32, bool PAIR>
+template <bool GROUPED, bool OUT_F32, bool PAIR, bool RS>
 __global__ void __launch_bounds__(THREADS, 1)
 fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                             const __grid_constant__ CUtensorMap map_b, const GemmArgs p)
 {
-    using L = Layout<GROUPED, PAIR>;
+    using L = Layout<GROUPED, PAIR, RS>;
     constexpr int STAGES = L::STAGES;
     constexpr int CL = L::CL;
     extern __shared__ uint8_t smem_raw[];
@@ -441,6 +451,9 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                 const bool wv = lane < 2 && nb < p.NB;
                 const float* w_base =
                     p.w_s + (static_cast<int64_t>(ti.g) * p.NB + (wv ? nb : 0)) * KB;
+                bool cv[RS ? 8 : 1];                         // RS: B rows n0 + lane + 32 q exist
+#pragma unroll
+                for (int q = 0; q < (RS ? 8 : 1); q++) cv[q] = ti.n0 + lane + 32 * q < p.N;
                 for (int kb = 0; kb < KB; kb++, it++) {
                     const uint32_t slot = it % SCALE_SLOTS;
                     const uint32_t ph = (it / SCALE_SLOTS) & 1u;
@@ -450,14 +463,22 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                         ok = false;
                         break;
                     }
-                    const uint32_t dst = scl0 + slot * SCALE_SLOT_BYTES;
+                    const uint32_t dst = scl0 + slot * L::SLOT;
                     const float* a_row = p.a_s + static_cast<int64_t>(kb) * p.rows + ti.row0;
 #pragma unroll
                     for (int q = 0; q < 4; q++)
                         cp_async_4(dst + (lane + 32 * q) * 4,
                                    rv[q] ? a_row + lane + 32 * q : zero_src, rv[q] ? 4u : 0u);
-                    if (lane < 2)
+                    if constexpr (RS) {
+                        // the 256 B-row scales of this K block: b_s[kb][n0 .. n0 + 255]
+                        const float* b_row = p.w_s + static_cast<int64_t>(kb) * p.N + ti.n0;
+#pragma unroll
+                        for (int q = 0; q < 8; q++)
+                            cp_async_4(dst + 512 + (lane + 32 * q) * 4,
+                                       cv[q] ? b_row + lane + 32 * q : zero_src, cv[q] ? 4u : 0u);
+                    } else if (lane < 2) {
                         cp_async_4(dst + 512 + lane * 4, wv ? w_base + kb : zero_src, wv ? 4u : 0u);
+                    }
                     cp_async_mbar_arrive(sfull0 + 8 * slot);
                 }
             }
@@ -498,11 +519,18 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     ok = false;
                     break;
                 }
-                const uint32_t sl = scl0 + slot * SCALE_SLOT_BYTES;
-                const float sc =
-                    __fmul_rn(ld_shared_f32(sl + r * 4), ld_shared_f32(sl + 512 + half * 4));
-                __syncwarp();
-                if (lane == 0) mbar_arrive(sempty0 + 8 * slot);
+                const uint32_t sl = scl0 + slot * L::SLOT;
+                // Block-scaled B: one product s_a[row] * s_w[block] per K block. RS: s_a[row]
+                // here, times s_b[column] per column pair below (B-row scales stay in the slot
+                // until the promotion is done).
+                const float sc = RS ? ld_shared_f32(sl + r * 4)
+                                    : __fmul_rn(ld_shared_f32(sl + r * 4),
+                                                ld_shared_f32(sl + 512 + half * 4));
+                const uint32_t sb = sl + 512 + half * 128 * 4;   // RS: s_b of this half's columns
+                if constexpr (!RS) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(sempty0 + 8 * slot);
+                }
 
                 const uint32_t b = j & 1u;
                 const uint32_t pb = (j >> 1) & 1u;
@@ -517,25 +545,52 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                 // is promoted (two register buffers of 16 packed pairs).
                 const uint32_t taddr = tmem_base + t_lane + b * BN + half * 128;
                 const uint64_t sc2 = f32x2_splat(sc);
-                uint64_t v0[16], v1[16];
-                tmem_ld_32cols(taddr, v0);
-                tmem_wait_ld(v0);
-                tmem_ld_32cols(taddr + 32, v1);
+                if constexpr (RS) {
+                    // Per-column scales, eight 16-column chunks: acc = fma(P * s_b[n], s_a[m], acc)
+                    // (the product P * s_b depends on the TMEM data, so it is formed only when
+                    // the chunk has arrived instead of being computed ahead into registers).
+                    uint64_t u0[8], u1[8];
+                    tmem_ld_16cols(taddr, u0);
 #pragma unroll
-                for (int i = 0; i < 16; i++) ffma2(acc[i], v0[i], sc2);
-                tmem_wait_ld(v1);
-                tmem_ld_32cols(taddr + 64, v0);
+                    for (int c = 0; c < 8; c += 2) {
+                        __syncwarp();   // with the form above, keeps the epilogue within its registers
+                        tmem_wait_ld(u0);
+                        tmem_ld_16cols(taddr + 16 * (c + 1), u1);
 #pragma unroll
-                for (int i = 0; i < 16; i++) ffma2(acc[16 + i], v1[i], sc2);
-                tmem_wait_ld(v0);
-                tmem_ld_32cols(taddr + 96, v1);
+                        for (int i = 0; i < 8; i++)
+                            ffma2(acc[8 * c + i], fmul2(u0[i], ld_shared_u64(sb + 64 * c + 8 * i)),
+                                  sc2);
+                        tmem_wait_ld(u1);
+                        if (c + 2 < 8) tmem_ld_16cols(taddr + 16 * (c + 2), u0);
 #pragma unroll
-                for (int i = 0; i < 16; i++) ffma2(acc[32 + i], v0[i], sc2);
-                tmem_wait_ld(v1);
+                        for (int i = 0; i < 8; i++)
+                            ffma2(acc[8 * (c + 1) + i],
+                                  fmul2(u1[i], ld_shared_u64(sb + 64 * (c + 1) + 8 * i)), sc2);
+                    }
+                } else {
+                    uint64_t v0[16], v1[16];
+                    tmem_ld_32cols(taddr, v0);
+                    tmem_wait_ld(v0);
+                    tmem_ld_32cols(taddr + 32, v1);
 #pragma unroll
-                for (int i = 0; i < 16; i++) ffma2(acc[48 + i], v1[i], sc2);
+                    for (int i = 0; i < 16; i++) ffma2(acc[i], v0[i], sc2);
+                    tmem_wait_ld(v1);
+                    tmem_ld_32cols(taddr + 64, v0);
+#pragma unroll
+                    for (int i = 0; i < 16; i++) ffma2(acc[16 + i], v1[i], sc2);
+                    tmem_wait_ld(v0);
+                    tmem_ld_32cols(taddr + 96, v1);
+#pragma unroll
+                    for (int i = 0; i < 16; i++) ffma2(acc[32 + i], v0[i], sc2);
+                    tmem_wait_ld(v1);
+#pragma unroll
+                    for (int i = 0; i < 16; i++) ffma2(acc[48 + i], v1[i], sc2);
+                }
                 tc_fence_before();
                 __syncwarp();
+                if constexpr (RS) {
+                    if (lane == 0) mbar_arrive(sempty0 + 8 * slot);
+                }
                 // (test hook: one epilogue warp can be told to skip one release, see GemmArgs)
                 if (lane == 0 && !(warp == EPI_WARP0 && static_cast<int>(j) == p.fault_skip_release))
                     mbar_arrive(tempty0 + 8 * b);
@@ -601,13 +656,13 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     if constexpr (PAIR) cluster_sync();   // no CTA leaves while its peer still deallocates
 }
 
-template <bool GROUPED, bool OUT_F32, bool PAIR>
+template <bool GROUPED, bool OUT_F32, bool PAIR, bool RS>
 cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& args,
                        int max_ctas, cudaStream_t stream)
 {
     constexpr int CL = PAIR ? 2 : 1;
-    auto kern = fp8_blockscaled_gemm_kernel<GROUPED, OUT_F32, PAIR>;
-    const size_t smem = gemm_smem_bytes(GROUPED, args.G);
+    auto kern = fp8_blockscaled_gemm_kernel<GROUPED, OUT_F32, PAIR, RS>;
+    const size_t smem = gemm_smem_bytes(GROUPED, RS, args.G);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -643,25 +698,35 @@ cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const GemmA
 
 }  // namespace
 
-size_t gemm_smem_bytes(bool grouped, int G)
+size_t gemm_smem_bytes(bool grouped, bool row_scaled_b, int G)
 {
     constexpr bool DENSE_PAIR = GEMM_DENSE_CLUSTER == 2;
-    if (!grouped) return static_cast<size_t>(Layout<false, DENSE_PAIR>::GROUP_OFF) + ALIGN_PAD;
-    return static_cast<size_t>(Layout<true, false>::GROUP_OFF) + ALIGN_PAD +
+    if (row_scaled_b)
+        return static_cast<size_t>(Layout<false, DENSE_PAIR, true>::GROUP_OFF) + ALIGN_PAD;
+    if (!grouped)
+        return static_cast<size_t>(Layout<false, DENSE_PAIR, false>::GROUP_OFF) + ALIGN_PAD;
+    return static_cast<size_t>(Layout<true, false, false>::GROUP_OFF) + ALIGN_PAD +
            2 * static_cast<size_t>(G + 1) * sizeof(int);
 }
 
 int gemm_cluster_size(bool grouped) { return grouped ? 1 : GEMM_DENSE_CLUSTER; }
 
 cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args,
-                        bool grouped, bool out_f32, int max_ctas, cudaStream_t stream)
+                        GemmKind kind, bool out_f32, int max_ctas, cudaStream_t stream)
 {
-    constexpr bool DENSE_PAIR = GEMM_DENSE_CLUSTER == 2;
-    if (grouped)
-        return out_f32 ? launch_one<true, true, false>(map_a, map_b, args, max_ctas, stream)
-                       : launch_one<true, false, false>(map_a, map_b, args, max_ctas, stream);
-    return out_f32 ? launch_one<false, true, DENSE_PAIR>(map_a, map_b, args, max_ctas, stream)
-                   : launch_one<false, false, DENSE_PAIR>(map_a, map_b, args, max_ctas, stream);
+    constexpr bool DP = GEMM_DENSE_CLUSTER == 2;
+    switch (kind) {
+    case GemmKind::GROUPED:
+        return out_f32 ? launch_one<true, true, false, false>(map_a, map_b, args, max_ctas, stream)
+                       : launch_one<true, false, false, false>(map_a, map_b, args, max_ctas, stream);
+    case GemmKind::ROW_SCALED:
+        return out_f32 ? launch_one<false, true, DP, true>(map_a, map_b, args, max_ctas, stream)
+                       : launch_one<false, false, DP, true>(map_a, map_b, args, max_ctas, stream);
+    case GemmKind::DENSE:
+    default:
+        return out_f32 ? launch_one<false, true, DP, false>(map_a, map_b, args, max_ctas, stream)
+                       : launch_one<false, false, DP, false>(map_a, map_b, args, max_ctas, stream);
+    }
 }
 
 }  // namespace fp8bs

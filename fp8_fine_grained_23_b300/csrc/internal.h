@@ -55,15 +55,22 @@ cudaError_t launch_quant_act(const void* x, int64_t M, int64_t K, int64_t ldx, u
                              cudaStream_t stream);
 cudaError_t launch_quant_weight(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
                                 int64_t ldq, float* scales, cudaStream_t stream);
+cudaError_t launch_quant_act_128x1(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* qt,
+                                   int64_t ldqt, float* scales, cudaStream_t stream);
+cudaError_t launch_quant_weight_t(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* qt,
+                                  int64_t ldqt, float* scales_t, cudaStream_t stream);
 // max_ctas: the persistent grid's upper bound (the SM count); the launcher sizes the grid.
 // One-shot test hook (api.cu): the index for GemmArgs::fault_skip_release of the next grouped
 // GEMM launch, then back to -1.
 int take_fault_skip_release();
 
+// DENSE: per-128x128-block B scales; GROUPED: the same per expert; ROW_SCALED: a scale per B
+// row and K block (the 1d1d weight-gradient GEMM), dense only.
+enum class GemmKind { DENSE, GROUPED, ROW_SCALED };
 cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args,
-                        bool grouped, bool out_f32, int max_ctas, cudaStream_t stream);
+                        GemmKind kind, bool out_f32, int max_ctas, cudaStream_t stream);
 int gemm_cluster_size(bool grouped);
-size_t gemm_smem_bytes(bool grouped, int G);
+size_t gemm_smem_bytes(bool grouped, bool row_scaled_b, int G);
 
 // ------------------------------------------------------------------------------------
 // Host-side helpers of the C ABI (api.cu)

@@ -102,5 +102,5 @@ extern "C" int fp8_blockscaled_gemm_noalloc(const uint8_t* a_q, const float* a_s
         cudaGetLastError();
         return FP8BS_ERR_CUDA;
     }
-    return cuda_status(launch_gemm(ma, mb, args, false, out_dtype == FP8BS_OUT_F32, d->num_sms, s));
+    return cuda_status(launch_gemm(ma, mb, args, GemmKind::DENSE, out_dtype == FP8BS_OUT_F32, d->num_sms, s));
 }

@@ -384,6 +384,14 @@ __device__ __forceinline__ void ffma2(uint64_t& acc, uint64_t p, uint64_t s2)
     asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(p), "l"(s2));
 }
 
+// Packed FP32x2 multiply, each lane rounded to nearest even.
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 __device__ __forceinline__ float f32x2_lo(uint64_t v)
 {
     return __uint_as_float(static_cast<uint32_t>(v));

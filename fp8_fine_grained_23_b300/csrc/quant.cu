@@ -353,6 +353,126 @@ quant_weight_128x128_kernel(const uint16_t* __restrict__ w, int64_t N, int KB, i
     if (threadIdx.x == 0) scales[nb * KB + kb] = ts.s;
 }
 
+// ------------------------------------------------------------------------------------
+// Backward-pass quantizers with transposed codes (the pages use E4M3 for the backward pass
+// too: codingmall.com "Định dạng E4M3 hợp nhất", dtcms.com 三.2). A contraction over the rows
+// of the input needs the codes with those rows contiguous, so both write qt[c][r].
+//   PER_COLUMN (128x1 tiles): one scale per column of a 128x128 block, i.e. per 128 tokens of
+//     one channel, for the weight-gradient GEMM; scales[rb * scale_ld + c] (c = global column).
+//   else (128x128 blocks): one scale per block, the forward weight blocks laid out as W^T for
+//     the data-gradient GEMM; scales[cb * scale_ld + rb].
+// One CTA per 128x128 block (rb = blockIdx.y, cb = blockIdx.x). Thread t holds rows
+// 8 * (t >> 4) .. + 7 and columns 8 * (t & 15) .. + 7 (eight coalesced 16-byte loads). The
+// codes of one column are formed straight from the held values (eight rows -> eight bytes)
+// and staged in a 128 x 128-byte tile whose 16-byte chunk j of row c sits at j ^ ((c >> 3) & 7),
+// which keeps both the 8-byte writes and the 16-byte reads free of bank conflicts; the tile
+// then leaves as 128 rows of 128 contiguous bytes.
+// ------------------------------------------------------------------------------------
+template <bool PER_COLUMN>
+__global__ void __launch_bounds__(QUANT_THREADS)
+quant_transpose_kernel(const uint16_t* __restrict__ x, int64_t ldx, uint8_t* __restrict__ qt,
+                       int64_t ldqt, float* __restrict__ scales, int64_t scale_ld)
+{
+    __shared__ float red[QUANT_THREADS / 32][128];
+    __shared__ float col_r[128];
+    __shared__ uint32_t col_mode[128];   // bit 0: tiny amax, bit 1: zero tile
+    __shared__ __align__(16) uint8_t tile[128 * 128];
+
+    const int t = threadIdx.x;
+    const int c8 = t & 15;
+    const int rg = t >> 4;
+    const int lane = t & 31;
+    const int warp = t >> 5;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 128;
+    const int64_t c0 = static_cast<int64_t>(blockIdx.x) * 128;
+
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; i++)
+        v[i] = ld_stream_v4(x + (r0 + rg * 8 + i) * ldx + c0 + c8 * 8);
+
+    // |x| maxima: per column of this thread (PER_COLUMN) or over everything it holds.
+    float cm[8];
+#pragma unroll
+    for (int j = 0; j < 8; j++) cm[j] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+        float f[8];
+        unpack_bf16x8(v[i], f);
+#pragma unroll
+        for (int j = 0; j < 8; j++) cm[j] = fmaxf(cm[j], fabsf(f[j]));
+    }
+    if constexpr (PER_COLUMN) {
+        // lanes l and l ^ 16 hold the same columns (row groups 2w and 2w + 1)
+#pragma unroll
+        for (int j = 0; j < 8; j++) cm[j] = fmaxf(cm[j], __shfl_xor_sync(0xffffffffu, cm[j], 16));
+        if (lane < 16) {
+#pragma unroll
+            for (int j = 0; j < 8; j++) red[warp][c8 * 8 + j] = cm[j];
+        }
+        __syncthreads();
+        if (t < 128) {
+            float a = red[0][t];
+#pragma unroll
+            for (int w = 1; w < QUANT_THREADS / 32; w++) a = fmaxf(a, red[w][t]);
+            const TileScale ts = tile_scale(a);
+            col_r[t] = ts.r;
+            col_mode[t] = (ts.tiny ? 1u : 0u) | (ts.zero ? 2u : 0u);
+            scales[static_cast<int64_t>(blockIdx.y) * scale_ld + c0 + t] = ts.s;
+        }
+    } else {
+        float a = cm[0];
+#pragma unroll
+        for (int j = 1; j < 8; j++) a = fmaxf(a, cm[j]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+        if (lane == 0) red[warp][0] = a;
+        __syncthreads();
+        if (t == 0) {
+            a = red[0][0];
+#pragma unroll
+            for (int w = 1; w < QUANT_THREADS / 32; w++) a = fmaxf(a, red[w][0]);
+            const TileScale ts = tile_scale(a);
+            col_r[0] = ts.r;
+            col_mode[0] = (ts.tiny ? 1u : 0u) | (ts.zero ? 2u : 0u);
+            scales[static_cast<int64_t>(blockIdx.x) * scale_ld + blockIdx.y] = ts.s;
+        }
+    }
+    __syncthreads();
+
+    // Column c8 * 8 + j, rows rg * 8 .. + 7 -> eight code bytes (row order), one 8-byte store.
+    const uint32_t tile_base = smem_u32(tile);
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        const int c = c8 * 8 + j;
+        const float r = PER_COLUMN ? col_r[c] : col_r[0];
+        const uint32_t mode = PER_COLUMN ? col_mode[c] : col_mode[0];
+        float y[8];
+#pragma unroll
+        for (int i = 0; i < 8; i++) {
+            const uint32_t wd = (j & 2) ? ((j & 4) ? v[i].w : v[i].y) : ((j & 4) ? v[i].z : v[i].x);
+            const float f = __uint_as_float((j & 1) ? (wd & 0xFFFF0000u) : (wd << 16));
+            y[i] = (mode & 1u) ? __fmul_rn(__fmul_rn(f, 0x1p64f), r) : __fmul_rn(f, r);
+        }
+        uint32_t w0 = cvt_e4m3x2(y[0], y[1]) | (cvt_e4m3x2(y[2], y[3]) << 16);
+        uint32_t w1 = cvt_e4m3x2(y[4], y[5]) | (cvt_e4m3x2(y[6], y[7]) << 16);
+        if (mode & 2u) w0 = w1 = 0u;
+        const uint32_t chunk = static_cast<uint32_t>((rg >> 1) ^ (c8 & 7));
+        st_shared_v2(tile_base + c * 128 + chunk * 16 + (rg & 1) * 8, make_uint2(w0, w1));
+    }
+    __syncthreads();
+
+    // 128 rows of 128 bytes: thread t writes chunks (t + 256 p), eight threads per row.
+#pragma unroll
+    for (int pass = 0; pass < 4; pass++) {
+        const int idx = pass * QUANT_THREADS + t;
+        const int c = idx >> 3;
+        const int q = idx & 7;
+        const uint4 val = ld_shared_v4(tile_base + c * 128 + ((q ^ ((c >> 3) & 7)) * 16));
+        st_global_v4(qt + (c0 + c) * ldqt + r0 + q * 16, val);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_quant_act(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
@@ -387,6 +507,24 @@ cudaError_t launch_quant_weight(const void* w, int64_t N, int64_t K, int64_t ldw
     dim3 grid(KB, static_cast<unsigned>(NB));
     quant_weight_128x128_kernel<<<grid, QUANT_THREADS, 0, stream>>>(
         static_cast<const uint16_t*>(w), N, KB, ldw, q, ldq, scales);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_act_128x1(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* qt,
+                                   int64_t ldqt, float* scales, cudaStream_t stream)
+{
+    dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>(M / 128));
+    quant_transpose_kernel<true><<<grid, QUANT_THREADS, 0, stream>>>(
+        static_cast<const uint16_t*>(x), ldx, qt, ldqt, scales, K);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_weight_t(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* qt,
+                                  int64_t ldqt, float* scales_t, cudaStream_t stream)
+{
+    dim3 grid(static_cast<unsigned>(K / 128), static_cast<unsigned>(N / 128));
+    quant_transpose_kernel<false><<<grid, QUANT_THREADS, 0, stream>>>(
+        static_cast<const uint16_t*>(w), ldw, qt, ldqt, scales_t, N / 128);
     return cudaGetLastError();
 }
 

@@ -29,13 +29,17 @@ lib.fp8_blockscaled_gemm_noalloc.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, _
                                              _p]
 lib.fp8_blockscaled_grouped_gemm.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64, _i64, _p,
                                              _i64, _int, _p]
+lib.fp8_quant_act_128x1.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p, _p]
+lib.fp8_quant_weight_128x128_t.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p, _p]
+lib.fp8_blockscaled_gemm_1d1d.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, _p, _i64, _int, _p]
 lib.fp8bs_status_string.argtypes = [_int]
 lib.fp8bs_status_string.restype = ctypes.c_char_p
 lib.fp8bs_last_error.argtypes = [_p]
 lib.fp8bs_debug_skip_release.argtypes = [_int]
 for _f in (lib.fp8_quant_act_1x128, lib.fp8_quant_weight_128x128, lib.fp8_blockscaled_gemm,
            lib.fp8_blockscaled_gemm_noalloc, lib.fp8_blockscaled_grouped_gemm,
-           lib.fp8bs_last_error, lib.fp8bs_debug_skip_release):
+           lib.fp8bs_last_error, lib.fp8bs_debug_skip_release, lib.fp8_quant_act_128x1,
+           lib.fp8_quant_weight_128x128_t, lib.fp8_blockscaled_gemm_1d1d):
     _f.restype = _int
 
 FP8BS_OK = 0
@@ -113,6 +117,44 @@ def fp8_quant_weight_128x128(w: torch.Tensor, q: torch.Tensor | None = None,
     return q, scales
 
 
+def fp8_quant_act_128x1(x: torch.Tensor, qt: torch.Tensor | None = None,
+                        scales: torch.Tensor | None = None, stream=None):
+    """Backward 128x1 tiles of BF16 x [M][K] (M % 128 == 0): codes transposed, qt [K][M], and
+    FP32 scales [M/128][K]."""
+    if x.dtype != torch.bfloat16:
+        raise TypeError("x must be bfloat16")
+    M, ldx = _rows_ld(x, "x")
+    K = x.shape[1]
+    if qt is None:
+        qt = torch.empty(K, M, dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(M // 128, K, dtype=torch.float32, device=x.device)
+    _, ldqt = _rows_ld(qt, "qt")
+    _check("fp8_quant_act_128x1",
+           lib.fp8_quant_act_128x1(x.data_ptr(), M, K, ldx, qt.data_ptr(), ldqt,
+                                   scales.data_ptr(), _stream(stream)))
+    return qt, scales
+
+
+def fp8_quant_weight_128x128_t(w: torch.Tensor, qt: torch.Tensor | None = None,
+                               scales_t: torch.Tensor | None = None, stream=None):
+    """128x128 blocks of BF16 w [N][K] with the codes written as W^T: qt [K][N] and FP32
+    scales_t [K/128][N/128]."""
+    if w.dtype != torch.bfloat16:
+        raise TypeError("w must be bfloat16")
+    N, ldw = _rows_ld(w, "w")
+    K = w.shape[1]
+    if qt is None:
+        qt = torch.empty(K, N, dtype=torch.uint8, device=w.device)
+    if scales_t is None:
+        scales_t = torch.empty(K // 128, N // 128, dtype=torch.float32, device=w.device)
+    _, ldqt = _rows_ld(qt, "qt")
+    _check("fp8_quant_weight_128x128_t",
+           lib.fp8_quant_weight_128x128_t(w.data_ptr(), N, K, ldw, qt.data_ptr(), ldqt,
+                                          scales_t.data_ptr(), _stream(stream)))
+    return qt, scales_t
+
+
 def _out_code(dtype) -> int:
     if dtype == torch.bfloat16:
         return FP8BS_OUT_BF16
@@ -134,6 +176,22 @@ def fp8_blockscaled_gemm(a_q: torch.Tensor, a_s: torch.Tensor, w_q: torch.Tensor
            lib.fp8_blockscaled_gemm(a_q.data_ptr(), a_s.data_ptr(), w_q.data_ptr(),
                                     w_s.data_ptr(), M, N, K, out.data_ptr(), ldc,
                                     _out_code(out.dtype), _stream(stream)))
+    return out
+
+
+def fp8_blockscaled_gemm_1d1d(a_q: torch.Tensor, a_s: torch.Tensor, b_q: torch.Tensor,
+                              b_s: torch.Tensor, out: torch.Tensor | None = None,
+                              out_dtype=torch.bfloat16, stream=None) -> torch.Tensor:
+    """C [M][N] = A B^T with per-row scales on both operands: a_s [K/128][M], b_s [K/128][N]."""
+    M, K = a_q.shape
+    N = b_q.shape[0]
+    if out is None:
+        out = torch.empty(M, N, dtype=out_dtype, device=a_q.device)
+    _, ldc = _rows_ld(out, "out")
+    _check("fp8_blockscaled_gemm_1d1d",
+           lib.fp8_blockscaled_gemm_1d1d(a_q.data_ptr(), a_s.data_ptr(), b_q.data_ptr(),
+                                         b_s.data_ptr(), M, N, K, out.data_ptr(), ldc,
+                                         _out_code(out.dtype), _stream(stream)))
     return out
 
 

@@ -13,6 +13,9 @@ Recipe (every workload):
 The CPU and CUDA generators give different streams for the same seed: a test that compares
 the GPU path with the oracle draws once and hands the same BF16 tensor to both.
 
+Backward pass (dense workloads): the output gradient dY [M][N] is drawn like activations and
+scaled by 2^-12, from its own generator (the workload's seed + 1000).
+
 MoE routing (grouped workload): expert popularity is proportional to rank^-1.1 with the rank a
 seeded permutation of the experts; every token picks 8 distinct experts by Gumbel-top-8 on the
 log-popularity (sampling without replacement); the routed rows are sorted by expert and the
@@ -138,6 +141,21 @@ def gemm_inputs(shape: GemmShape, device) -> tuple[torch.Tensor, torch.Tensor]:
         pad = torch.zeros(shape.n_padded - shape.N, shape.K, dtype=w.dtype, device=device)
         w = torch.cat([w, pad], dim=0)
     return a, w
+
+
+# Backward pass of a dense projection: X [M][K] and W [N][K] as in the forward workload of the
+# same shape, and the output gradient dY [M][N] drawn like activations (N(0, 1), 0.1% x100
+# outliers) then scaled by 2^-12 (exact in BF16), from its own generator (seed + 1000).
+GRAD_SIGMA = 2.0 ** -12
+GRAD_SEED_OFFSET = 1000
+
+
+def backward_inputs(shape: GemmShape, device) -> tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """(X [M][K], W [N][K], dY [M][N]) for the backward pass of a dense workload."""
+    x, w = gemm_inputs(shape, device)
+    g = generator(shape.seed + GRAD_SEED_OFFSET, device)
+    dy = activations(shape.M, shape.N, g, device, sigma=GRAD_SIGMA)
+    return x, w, dy
 
 
 def sweep_activations(M: int, device) -> torch.Tensor:

@@ -129,6 +129,64 @@ int fp8_blockscaled_grouped_gemm(const uint8_t *a_q, const float *a_s,
                                  fp8bs_stream_t stream);
 
 /*
+ * Backward pass. The pages use the same E4M3 format in the backward pass as in the forward
+ * pass ([codingmall] "Định dạng E4M3 hợp nhất"; [dtcms] 三.2) and name no backward tile shapes.
+ * Reading: a block-scaled contraction needs one scale per 128-long block of the contracted
+ * index, so
+ *   data gradient    dX[M][K] = dY[M][N] W[N][K]: fp8_quant_act_1x128 on dY, W as W^T codes
+ *                    in its 128x128 blocks (fp8_quant_weight_128x128_t), fp8_blockscaled_gemm;
+ *   weight gradient  dW[N][K] = dY^T X (contracting over the M tokens): dY and X in 128x1 tiles
+ *                    (fp8_quant_act_128x1), fp8_blockscaled_gemm_1d1d.
+ */
+
+/*
+ * 128x1 tiles: one scale per 128 consecutive rows of one column (128 tokens of one channel),
+ * with the codes written transposed so that the rows become the contiguous, contracted index.
+ *   x       BF16 [M][ldx], the first K columns are read.
+ *   qt      E4M3 codes [K][ldqt]: qt[k*ldqt + m] is the code of x[m][k].
+ *   scales  FP32 [M/128][K]: scales[mb*K + k] covers rows [128 mb, 128 mb + 128) of column k
+ *           (the a_s / b_s layout fp8_blockscaled_gemm_1d1d expects for an operand qt).
+ * Tile arithmetic as for every quantizer above. Requires M >= 0 (M == 0 is a no-op),
+ * M % 128 == 0, M / 128 <= 65535, K > 0, K % 128 == 0, ldx >= K, ldqt >= M, ldx % 8 == 0,
+ * ldqt % 16 == 0, x and qt 16-byte aligned, scales 4-byte aligned.
+ */
+int fp8_quant_act_128x1(const void *x, int64_t M, int64_t K, int64_t ldx,
+                        uint8_t *qt, int64_t ldqt, float *scales, fp8bs_stream_t stream);
+
+/*
+ * 128x128 weight blocks with the codes written as W^T, the B operand of the data-gradient GEMM
+ * (which contracts over N). The blocks, their scales and their codes are exactly those of
+ * fp8_quant_weight_128x128 on the same W; only the layout differs.
+ *   w         BF16 [N][ldw], the first K columns are read.
+ *   qt        E4M3 codes [K][ldqt]: qt[k*ldqt + n] is the code of w[n][k].
+ *   scales_t  FP32 [K/128][N/128]: scales_t[kb*(N/128) + nb] is the scale of block (nb, kb)
+ *             (the w_s layout fp8_blockscaled_gemm expects for a weight operand qt [K][N]).
+ * Requires N >= 0 (N == 0 is a no-op), N % 128 == 0, N / 128 <= 65535, K > 0, K % 128 == 0,
+ * ldw >= K, ldqt >= N, ldw % 8 == 0, ldqt % 16 == 0, w and qt 16-byte aligned, scales_t
+ * 4-byte aligned.
+ */
+int fp8_quant_weight_128x128_t(const void *w, int64_t N, int64_t K, int64_t ldw,
+                               uint8_t *qt, int64_t ldqt, float *scales_t, fp8bs_stream_t stream);
+
+/*
+ * Block-scaled FP8 GEMM with a per-row scale on both operands ("1d1d"; the weight-gradient
+ * GEMM), C = A B^T:
+ *   C[m][n] = sum_kb a_s[kb*M + m] * b_s[kb*N + n] * P[m][n][kb],
+ *   P[m][n][kb] = sum over k in [128 kb, 128 kb + 128) of decode(a_q[m][k]) * decode(b_q[n][k]).
+ * P is formed by the tensor cores in FP32 and promoted once per K block in FP32:
+ * acc = fma(P * b_s[kb][n], a_s[kb][m], acc), increasing kb.
+ *   a_q  E4M3 [M][K] (contiguous rows), a_s FP32 [K/128][M]
+ *   b_q  E4M3 [N][K] (contiguous rows), b_s FP32 [K/128][N]
+ *   c    [M][ldc] BF16 or FP32, as for fp8_blockscaled_gemm.
+ * For dW = dY^T X: a = fp8_quant_act_128x1(dY) (M = channels of dY), b = fp8_quant_act_128x1(X)
+ * (N = channels of X), K = tokens. Requirements as for fp8_blockscaled_gemm.
+ */
+int fp8_blockscaled_gemm_1d1d(const uint8_t *a_q, const float *a_s,
+                              const uint8_t *b_q, const float *b_s,
+                              int64_t M, int64_t N, int64_t K,
+                              void *c, int64_t ldc, int out_dtype, fp8bs_stream_t stream);
+
+/*
  * fp8_blockscaled_gemm_noalloc: the same dense block-scaled GEMM as fp8_blockscaled_gemm, for
  * callers that cannot let a library allocate device memory. The pages describe no such interface;
  * this entry point has no counterpart there.

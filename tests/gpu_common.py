@@ -97,3 +97,45 @@ def assert_within_tolerance(c_gpu: np.ndarray, c64: np.ndarray, cabs: np.ndarray
 
 def gpu_bits_pair(a: torch.Tensor, w: torch.Tensor):
     return bits_of(a), bits_of(w)
+
+
+def _column_cuts(n_blocks: int) -> np.ndarray:
+    return np.linspace(0, n_blocks, min(THREADS, n_blocks) + 1).astype(int) * 128
+
+
+def oracle_quant_act_128x1(x_bits: np.ndarray):
+    """Oracle 128x1 quantization of [M][K] BF16 bits; column slabs of 128 on host threads.
+    Returns (codes [K][M], scales [M/128][K])."""
+    K = x_bits.shape[1]
+    if x_bits.size < (1 << 22):
+        return O.quant_act_128x1(x_bits)
+    cuts = _column_cuts(K // 128)
+    with ThreadPoolExecutor(THREADS) as ex:
+        parts = list(ex.map(lambda i: O.quant_act_128x1(x_bits[:, cuts[i]:cuts[i + 1]]),
+                            range(len(cuts) - 1)))
+    return np.concatenate([p[0] for p in parts]), np.concatenate([p[1] for p in parts], axis=1)
+
+
+def oracle_quant_weight_t(w_bits: np.ndarray):
+    """Oracle transposed 128x128 quantization of [N][K]; row-block slabs on host threads.
+    Returns (codes [K][N], scales [K/128][N/128])."""
+    N = w_bits.shape[0]
+    if w_bits.size < (1 << 22):
+        return O.quant_weight_128x128_t(w_bits)
+    cuts = _column_cuts(N // 128)
+    with ThreadPoolExecutor(THREADS) as ex:
+        parts = list(ex.map(lambda i: O.quant_weight_128x128_t(w_bits[cuts[i]:cuts[i + 1]]),
+                            range(len(cuts) - 1)))
+    return (np.concatenate([p[0] for p in parts], axis=1),
+            np.concatenate([p[1] for p in parts], axis=1))
+
+
+def oracle_points_1d1d(aq, a_s, bq, b_s, pm, pn):
+    """Oracle per-row-scaled GEMM elements at (pm[i], pn[i]) split over host threads."""
+    n = pm.size
+    cuts = np.linspace(0, n, THREADS + 1).astype(int)
+    with ThreadPoolExecutor(THREADS) as ex:
+        parts = list(ex.map(
+            lambda i: O.gemm_1d1d_points(aq, a_s, bq, b_s, pm[cuts[i]:cuts[i + 1]],
+                                         pn[cuts[i]:cuts[i + 1]]), range(THREADS)))
+    return np.concatenate([p[0] for p in parts]), np.concatenate([p[1] for p in parts])

@@ -27,7 +27,8 @@ def declared_functions():
 def test_header_declares_the_hot_path_calls():
     names = declared_functions()
     for n in ("fp8_quant_act_1x128", "fp8_quant_weight_128x128", "fp8_blockscaled_gemm",
-              "fp8_blockscaled_grouped_gemm", "fp8bs_status_string", "fp8bs_last_error"):
+              "fp8_blockscaled_grouped_gemm", "fp8bs_status_string", "fp8bs_last_error",
+              "fp8_quant_act_128x1", "fp8_quant_weight_128x128_t", "fp8_blockscaled_gemm_1d1d"):
         assert n in names
 
 
@@ -90,6 +91,34 @@ def test_grouped_gemm_argument_checks(F):
     assert g(P16, P4, P16, P4, None, 2, 8, 32, 128, P16, 32, 0, None) == -1    # no offsets
     assert g(P16, P4, P16, P4, P4 + 1, 2, 8, 32, 128, P16, 32, 0, None) == -2
     assert g(P16, P4, P16, P4, P4, 2, 0, 32, 128, P16, 32, 0, None) == 0       # R == 0
+
+
+@pytest.mark.parametrize("fn", ["fp8_quant_act_128x1", "fp8_quant_weight_128x128_t"])
+@pytest.mark.parametrize("args,expect", [
+    ((P16, 200, 128, 128, P16, 208, P4), -1),     # rows % 128 != 0 (the contracted index)
+    ((P16, 256, 100, 128, P16, 256, P4), -1),     # K % 128 != 0
+    ((P16, 256, 128, 128, P16, 128, P4), -1),     # ldqt < rows
+    ((P16, 256, 128, 64, P16, 256, P4), -1),      # ld_in < K
+    ((P16, 128 * 65536, 128, 128, P16, 128 * 65536, P4), -1),   # grid limit on row blocks
+    ((None, 256, 128, 128, P16, 256, P4), -1),    # null input
+    ((P16 + 2, 256, 128, 128, P16, 256, P4), -2), # misaligned input
+    ((P16, 256, 128, 128, P16, 264, P4), -2),     # ldqt % 16 != 0
+    ((P16, 256, 128, 128, P16, 256, P4 + 1), -2), # misaligned scales
+    ((P16, 0, 128, 128, P16, 0, P4), 0),          # no rows: no-op
+])
+def test_transpose_quant_argument_checks(F, fn, args, expect):
+    assert getattr(F.lib, fn)(*args, None) == expect
+
+
+@pytest.mark.parametrize("mnk,ldc,dt,expect", [
+    ((4, 24, 128), 24, 0, -1),
+    ((4, 32, 100), 32, 0, -1),
+    ((4, 32, 128), 36, 0, -2),
+    ((0, 32, 128), 32, 0, 0),
+])
+def test_gemm_1d1d_argument_checks(F, mnk, ldc, dt, expect):
+    M, N, K = mnk
+    assert F.lib.fp8_blockscaled_gemm_1d1d(P16, P4, P16, P4, M, N, K, P16, ldc, dt, None) == expect
 
 
 def test_debug_hook_rejects_negative_index(F):
