@@ -330,6 +330,62 @@ def _timed(fn, dev, iters=10, warm=3):
     return statistics.mean(a.elapsed_time(b) for a, b in times)
 
 
+def run_backward(F, dev, hbm, fp8_peak):
+    """Backward pass of the dense projection (M=4096 tokens, N=18432, K=7168): the four
+    quantizations a training step needs (dY and X in 128x1 tiles for the weight gradient, dY in
+    1x128 tiles and W as W^T codes for the data gradient) and the two GEMMs, each timed alone."""
+    shape = WL.DENSE
+    x, w, dy = WL.backward_inputs(shape, dev)
+    M, N, K = shape.M, shape.N, shape.K
+    res = {"workload": f"dense_bwd_{M}x{N}x{K}"}
+
+    def quant(name, fn, elems, bytes_per_elem):
+        ms = _timed(fn, dev)
+        gbs = elems * bytes_per_elem / (ms * 1e-3) / 1e9
+        res[name] = {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
+                     "frac_hbm": round(gbs / hbm, 4)}
+
+    dyt_q = torch.empty(N, M, dtype=torch.uint8, device=dev)
+    dyt_s = torch.empty(M // 128, N, dtype=torch.float32, device=dev)
+    xt_q = torch.empty(K, M, dtype=torch.uint8, device=dev)
+    xt_s = torch.empty(M // 128, K, dtype=torch.float32, device=dev)
+    dy_q = torch.empty(M, N, dtype=torch.uint8, device=dev)
+    dy_s = torch.empty(N // 128, M, dtype=torch.float32, device=dev)
+    wt_q = torch.empty(K, N, dtype=torch.uint8, device=dev)
+    wt_s = torch.empty(K // 128, N // 128, dtype=torch.float32, device=dev)
+    quant("quant_128x1_dY", lambda: F.fp8_quant_act_128x1(dy, dyt_q, dyt_s), M * N, ACT_BYTES_PER_ELEM)
+    quant("quant_128x1_X", lambda: F.fp8_quant_act_128x1(x, xt_q, xt_s), M * K, ACT_BYTES_PER_ELEM)
+    quant("quant_1x128_dY", lambda: F.fp8_quant_act_1x128(dy, dy_q, dy_s), M * N, ACT_BYTES_PER_ELEM)
+    quant("quant_weight_t_W", lambda: F.fp8_quant_weight_128x128_t(w, wt_q, wt_s), N * K,
+          W_BYTES_PER_ELEM)
+    dw = torch.empty(N, K, dtype=torch.float32, device=dev)
+    dx = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+    for name, fn in (
+            ("wgrad_gemm_1d1d_f32", lambda: F.fp8_blockscaled_gemm_1d1d(dyt_q, dyt_s, xt_q, xt_s,
+                                                                         out=dw)),
+            ("dgrad_gemm_bf16", lambda: F.fp8_blockscaled_gemm(dy_q, dy_s, wt_q, wt_s, out=dx))):
+        ms = _timed(fn, dev)
+        tf = gemm_flops(M, N, K) / (ms * 1e-3) / 1e12
+        res[name] = {"us": round(ms * 1e3, 1), "TFLOP/s": round(tf, 1),
+                     "frac_fp8_peak": round(tf / fp8_peak, 4)}
+    res["gemm_shapes"] = {"wgrad_gemm_1d1d_f32": [N, K, M], "dgrad_gemm_bf16": [M, K, N]}
+    return res
+
+
+def backward_only(rank):
+    """The backward-pass measurements alone (rank 0 only; no step, no baseline)."""
+    if rank != 0:
+        return None
+    from fp8_fine_grained_23_b300 import fp8bs as F
+    dev = torch.device("cuda", 0)
+    peaks, _ = load_peaks()
+    line = {"backward": run_backward(F, dev, peaks["hbm_gbs"],
+                                     peaks["bf16_tflops"] * FP8_OVER_BF16)}
+    if F.fp8bs_last_error() != F.FP8BS_OK:
+        raise RuntimeError("a kernel reported a device-side timeout")
+    return line
+
+
 def run_extras(F, dev, peaks, fp8_peak):
     out = {"timing": "each kernel alone, L2 flushed (256 MB read) before every iteration, "
                      "mean of 10 after 3 warm-up"}
@@ -399,6 +455,7 @@ def run_extras(F, dev, peaks, fp8_peak):
         del a, aq, a_s, wq, w_s, c
         torch.cuda.empty_cache()
     out["moe_grouped_gemm"] = moe
+    out["backward"] = run_backward(F, dev, hbm, fp8_peak)
     if F.fp8bs_last_error() != F.FP8BS_OK:
         raise RuntimeError("a kernel reported a pipeline timeout in the extra workloads")
     return out
@@ -527,7 +584,9 @@ def main():
                     help="skip the oracle timing on the host cores")
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--no-extras", action="store_true",
-                    help="skip the quantizer sweep, MLA and MoE workloads")
+                    help="skip the quantizer sweep, MLA, MoE and backward workloads")
+    ap.add_argument("--backward-only", action="store_true",
+                    help="time only the backward-pass kernels (one JSON object), e.g. for ncu")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -539,7 +598,9 @@ def main():
             torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group(backend)
     try:
-        if args.impl == "reference":
+        if args.backward_only:
+            line = backward_only(rank) if args.impl == "ours" else None
+        elif args.impl == "reference":
             line = run_reference(args, rank, world)
         else:
             line = run_ours(args, rank, world, local_rank)
