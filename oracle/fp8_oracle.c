@@ -423,6 +423,16 @@ void orc_grouped_gemm_points(const uint8_t *aq, int64_t lda, const float *as,
     }
 }
 
+/* SwiGLU between the two expert GEMMs, h = silu(g) * u with silu(x) = x / (1 + e^-x), in FP64.
+ * A reading: the pages name DeepSeekMoE's routed experts but not the activation between their
+ * two GEMMs; DeepSeek-V3's expert FFN uses SwiGLU. For x below about -709, e^-x overflows to
+ * +inf and silu(x) is -0. */
+void orc_swiglu_f64(const double *g, const double *u, int64_t n, double *h)
+{
+    for (int64_t i = 0; i < n; i++)
+        h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];
+}
+
 /* Unquantized FP64 product of the BF16 inputs, C[m][n] = sum_k x[m,k] * w[n,k]; used only to
  * check the oracle itself against the quantization error bound. */
 void orc_gemm_unquantized_f64(const uint16_t *x, int64_t ldx, const uint16_t *w, int64_t ldw,

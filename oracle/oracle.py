@@ -67,11 +67,12 @@ def lib() -> ctypes.CDLL:
             L.orc_quant_weight_128x128_t.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p]
             L.orc_gemm_1d1d_points.argtypes = [_p, _i64, _p, _p, _i64, _p, _i64, _i64, _i64,
                                                _i64, _p, _p, _p, _p, _p]
+            L.orc_swiglu_f64.argtypes = [_p, _p, _i64, _p]
             for f in (L.orc_e4m3_encode_array, L.orc_e4m3_decode_array, L.orc_quant_act_1x128,
                       L.orc_quant_weight_128x128, L.orc_gemm_points, L.orc_gemm_f64,
                       L.orc_grouped_gemm_points, L.orc_gemm_unquantized_f64,
                       L.orc_quant_act_128x1, L.orc_quant_weight_128x128_t,
-                      L.orc_gemm_1d1d_points):
+                      L.orc_gemm_1d1d_points, L.orc_swiglu_f64):
                 f.restype = None
             _lib = L
         return _lib
@@ -231,6 +232,37 @@ def grouped_gemm_points(aq, a_s, wq, w_s, offsets, pr, pn):
     lib().orc_grouped_gemm_points(_ptr(aq), K, _ptr(a_s), _ptr(wq), K, _ptr(w_s), _ptr(off),
                                   G, R, N, K, n, _ptr(pr), _ptr(pn), _ptr(c), _ptr(cabs))
     return c, cabs
+
+
+def swiglu_f64(g, u) -> np.ndarray:
+    """h = silu(g) * u elementwise in FP64 (the expert FFN activation, a reading)."""
+    g, u = _c(g, np.float64), _c(u, np.float64)
+    assert g.shape == u.shape
+    h = np.empty(g.shape, np.float64)
+    lib().orc_swiglu_f64(_ptr(g), _ptr(u), g.size, _ptr(h))
+    return h
+
+
+def gate_up_columns(I: int) -> tuple[np.ndarray, np.ndarray]:
+    """Columns of the gate and up outputs of channel c (0 <= c < I) in a gate/up GEMM whose
+    weight rows are interleaved in blocks of 128: gate 256 (c // 128) + c % 128, up + 128."""
+    c = np.arange(I, dtype=np.int64)
+    gate = 256 * (c // 128) + c % 128
+    return gate, gate + 128
+
+
+def grouped_swiglu_rows(aq, a_s, wq, w_s, offsets, rows):
+    """FP64 reference of the fused grouped gate/up GEMM + SwiGLU for whole rows: returns
+    (h, g, gabs, u, uabs), each [len(rows)][I], from the grouped GEMM oracle."""
+    rows = _c(rows, np.int64)
+    I = wq.shape[1] // 2
+    gc, uc = gate_up_columns(I)
+    pr = np.repeat(rows, I)
+    g, gabs = grouped_gemm_points(aq, a_s, wq, w_s, offsets, pr, np.tile(gc, rows.size))
+    u, uabs = grouped_gemm_points(aq, a_s, wq, w_s, offsets, pr, np.tile(uc, rows.size))
+    shape = (rows.size, I)
+    g, gabs, u, uabs = (x.reshape(shape) for x in (g, gabs, u, uabs))
+    return swiglu_f64(g, u), g, gabs, u, uabs
 
 
 def gemm_unquantized_f64(x_bits, w_bits) -> np.ndarray:
