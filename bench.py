@@ -424,12 +424,15 @@ def run_extras(F, dev, peaks, fp8_peak):
                            "frac_fp8_peak": round(tf / fp8_peak, 4), "N_run": w.shape[0]}
         del a, w, aq, a_s, wq, w_s, c
     out["mla_gemm"] = mla
-    # MoE grouped GEMMs
+    # MoE grouped GEMMs: gate+up and down alone (BF16 out), the gate+up GEMM with the fused
+    # SwiGLU + 1x128 re-quantization, and the expert FFN chain (fused gate+up, then down on h)
     moe = {}
     shape = WL.MOE
     off, token_of_row = WL.moe_routing(shape)
     R = int(off[-1])
     offs = torch.from_numpy(off).to(dev)
+    E = shape.experts
+    ops = {}
     for which in ("gate_up", "down"):
         if which == "gate_up":
             N, K = shape.n_gate_up, shape.hidden
@@ -440,9 +443,9 @@ def run_extras(F, dev, peaks, fp8_peak):
         wts = WL.moe_expert_weights(shape, N, K, which, dev)
         aq, a_s = F.fp8_quant_act_1x128(a)
         wq, w_s = F.fp8_quant_weight_128x128(wts.view(-1, K))
-        del wts
-        wq = wq.view(shape.experts, N, K)
-        w_s = w_s.view(shape.experts, N // 128, K // 128)
+        del wts, a
+        wq = wq.view(E, N, K)
+        w_s = w_s.view(E, N // 128, K // 128)
         c = torch.empty(R, N, dtype=torch.bfloat16, device=dev)
         ms = _timed(lambda: F.fp8_blockscaled_grouped_gemm(aq, a_s, wq, w_s, offs, out=c), dev)
         tf = gemm_flops(R, N, K) / (ms * 1e-3) / 1e12
@@ -451,9 +454,39 @@ def run_extras(F, dev, peaks, fp8_peak):
         moe[which] = {"us": round(ms * 1e3, 1), "TFLOP/s": round(tf, 1),
                       "frac_fp8_peak": round(tf / fp8_peak, 4), "GB/s": round(gbs, 1),
                       "frac_hbm": round(gbs / hbm, 4), "R": R, "N": N, "K": K,
-                      "experts": shape.experts}
-        del a, aq, a_s, wq, w_s, c
+                      "experts": E}
+        ops[which] = (aq, a_s, wq, w_s)
+        del c
         torch.cuda.empty_cache()
+    aq, a_s, wq, w_s = ops["gate_up"]
+    N2, I = shape.n_gate_up, shape.n_gate_up // 2
+    hq = torch.empty(R, I, dtype=torch.uint8, device=dev)
+    hs = torch.empty(I // 128, R, dtype=torch.float32, device=dev)
+    fused = lambda: F.fp8_blockscaled_grouped_gemm_swiglu_quant(aq, a_s, wq, w_s, offs, hq, hs)
+    ms = _timed(fused, dev)
+    algo_bytes = wq.numel() + aq.numel() + a_s.numel() * 4 + w_s.numel() * 4 + hq.numel() + \
+        hs.numel() * 4
+    gbs = algo_bytes / (ms * 1e-3) / 1e9
+    moe["gate_up_swiglu_quant"] = {
+        "us": round(ms * 1e3, 1), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4),
+        "TFLOP/s": round(gemm_flops(R, N2, shape.hidden) / (ms * 1e-3) / 1e12, 1),
+        "out": "E4M3 h [R][N2/2] + 1x128 scales (gate/up weight rows interleaved per 128)"}
+    dq, ds_, dwq, dws = ops["down"]
+    y = torch.empty(R, shape.hidden, dtype=torch.bfloat16, device=dev)
+
+    def chain():
+        fused()
+        F.fp8_blockscaled_grouped_gemm(hq, hs, dwq, dws, offs, out=y)
+    ms = _timed(chain, dev)
+    chain_bytes = algo_bytes + dwq.numel() + dws.numel() * 4 + y.numel() * 2
+    gbs = chain_bytes / (ms * 1e-3) / 1e9
+    moe["ffn_chain_fused"] = {
+        "us": round(ms * 1e3, 1), "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4),
+        "TFLOP/s": round((gemm_flops(R, N2, shape.hidden) + gemm_flops(R, shape.hidden, I)) /
+                         (ms * 1e-3) / 1e12, 1),
+        "steps": "gate/up GEMM + SwiGLU + 1x128 re-quantization, then the down GEMM on h"}
+    del ops, aq, a_s, wq, w_s, dq, ds_, dwq, dws, hq, hs, y
+    torch.cuda.empty_cache()
     out["moe_grouped_gemm"] = moe
     out["backward"] = run_backward(F, dev, hbm, fp8_peak)
     if F.fp8bs_last_error() != F.FP8BS_OK:

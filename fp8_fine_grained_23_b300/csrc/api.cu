@@ -196,6 +196,53 @@ int dense_gemm(GemmKind kind, const uint8_t* a_q, const float* a_s, const uint8_
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// Grouped launch shared by the plain grouped GEMM and the SwiGLU + re-quantizing one; the
+// caller has checked the output arguments (and that R > 0).
+int grouped_gemm(GemmKind kind, const uint8_t* a_q, const float* a_s, const uint8_t* w_q,
+                 const float* w_s, const int32_t* group_offsets, int64_t G, int64_t R, int64_t N,
+                 int64_t K, void* c, int64_t ldc, bool out_f32, float* h_s,
+                 fp8bs_stream_t stream)
+{
+    int st = FP8BS_OK;
+    if (!group_offsets) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned4(group_offsets)) return FP8BS_ERR_MISALIGNED;
+    if (G * N > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
+    DeviceInfo* d = nullptr;
+    if ((st = current_device(&d)) != FP8BS_OK) return st;
+    if ((st = ensure_error_word(d)) != FP8BS_OK) return st;
+    if ((st = ensure_encoder()) != FP8BS_OK) return st;
+
+    CUtensorMap ma, mb;
+    if ((st = make_code_map(&ma, a_q, K, R, K, GEMM_BM)) != FP8BS_OK) return st;
+    if ((st = make_code_map(&mb, w_q, K, G * N, K, GEMM_BN)) != FP8BS_OK) return st;
+
+    GemmArgs args{};
+    args.a_s = a_s;
+    args.w_s = w_s;
+    args.c = c;
+    args.ldc = ldc;
+    args.rows = R;
+    args.N = static_cast<int>(N);
+    args.KB = static_cast<int>(K / 128);
+    args.NB = static_cast<int>((N + 127) / 128);
+    args.NT = static_cast<int>((N + GEMM_BN - 1) / GEMM_BN);
+    args.MT = 0;
+    args.num_tiles = 0;
+    args.offsets = group_offsets;
+    args.h_s = h_s;
+    args.G = static_cast<int>(G);
+    args.err = d->err;
+    args.budget = wait_budget();
+    args.fault_skip_release = take_fault_skip_release();
+    // At most ceil(R/128) + G m-tiles exist across the groups; the exact count is formed on the
+    // device from the offsets, and CTAs without a tile exit at once.
+    const int64_t bound = ((R + GEMM_BM - 1) / GEMM_BM + G) * args.NT;
+    if (bound > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
+    const int max_ctas = static_cast<int>(bound < d->num_sms ? bound : d->num_sms);
+    return cuda_status(
+        launch_gemm(ma, mb, args, kind, out_f32, max_ctas, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace host
 
 int take_fault_skip_release()
@@ -280,42 +327,27 @@ int fp8_blockscaled_grouped_gemm(const uint8_t* a_q, const float* a_s, const uin
     if (G < 1 || G > GEMM_MAX_GROUPS) return FP8BS_ERR_INVALID_ARG;
     int st = check_gemm_args(a_q, a_s, w_q, w_s, R, N, K, c, ldc, out_dtype);
     if (st != FP8BS_OK || R == 0) return st;
-    if (!group_offsets) return FP8BS_ERR_INVALID_ARG;
-    if (!aligned4(group_offsets)) return FP8BS_ERR_MISALIGNED;
-    if (G * N > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
-    DeviceInfo* d = nullptr;
-    if ((st = current_device(&d)) != FP8BS_OK) return st;
-    if ((st = ensure_error_word(d)) != FP8BS_OK) return st;
-    if ((st = ensure_encoder()) != FP8BS_OK) return st;
+    return fp8bs::host::grouped_gemm(GemmKind::GROUPED, a_q, a_s, w_q, w_s, group_offsets, G, R,
+                                     N, K, c, ldc, out_dtype == FP8BS_OUT_F32, nullptr, stream);
+}
 
-    CUtensorMap ma, mb;
-    if ((st = make_code_map(&ma, a_q, K, R, K, GEMM_BM)) != FP8BS_OK) return st;
-    if ((st = make_code_map(&mb, w_q, K, G * N, K, GEMM_BN)) != FP8BS_OK) return st;
-
-    GemmArgs args{};
-    args.a_s = a_s;
-    args.w_s = w_s;
-    args.c = c;
-    args.ldc = ldc;
-    args.rows = R;
-    args.N = static_cast<int>(N);
-    args.KB = static_cast<int>(K / 128);
-    args.NB = static_cast<int>((N + 127) / 128);
-    args.NT = static_cast<int>((N + GEMM_BN - 1) / GEMM_BN);
-    args.MT = 0;
-    args.num_tiles = 0;
-    args.offsets = group_offsets;
-    args.G = static_cast<int>(G);
-    args.err = d->err;
-    args.budget = wait_budget();
-    args.fault_skip_release = take_fault_skip_release();
-    // At most ceil(R/128) + G m-tiles exist across the groups; the exact count is formed on the
-    // device from the offsets, and CTAs without a tile exit at once.
-    const int64_t bound = ((R + GEMM_BM - 1) / GEMM_BM + G) * args.NT;
-    if (bound > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
-    const int max_ctas = static_cast<int>(bound < d->num_sms ? bound : d->num_sms);
-    return cuda_status(launch_gemm(ma, mb, args, GemmKind::GROUPED, out_dtype == FP8BS_OUT_F32, max_ctas,
-                                   reinterpret_cast<cudaStream_t>(stream)));
+int fp8_blockscaled_grouped_gemm_swiglu_quant(const uint8_t* a_q, const float* a_s,
+                                              const uint8_t* w_q, const float* w_s,
+                                              const int32_t* group_offsets, int64_t G, int64_t R,
+                                              int64_t N2, int64_t K, uint8_t* h_q, int64_t ldh,
+                                              float* h_s, fp8bs_stream_t stream)
+{
+    if (G < 1 || G > GEMM_MAX_GROUPS) return FP8BS_ERR_INVALID_ARG;
+    if (R < 0 || N2 <= 0 || N2 % 256 != 0 || K <= 0 || K % 128 != 0 || ldh < N2 / 2)
+        return FP8BS_ERR_INVALID_ARG;
+    if (R > INT32_MAX || N2 > INT32_MAX || K > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
+    if (R == 0) return FP8BS_OK;
+    if (!a_q || !a_s || !w_q || !w_s || !h_q || !h_s) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned16(a_q) || !aligned16(w_q) || !aligned16(h_q) || !aligned4(a_s) ||
+        !aligned4(w_s) || !aligned4(h_s) || ldh % 16 != 0)
+        return FP8BS_ERR_MISALIGNED;
+    return fp8bs::host::grouped_gemm(GemmKind::GROUPED_SWIGLU, a_q, a_s, w_q, w_s, group_offsets,
+                                     G, R, N2, K, h_q, ldh, false, h_s, stream);
 }
 
 int fp8bs_debug_skip_release(int at)

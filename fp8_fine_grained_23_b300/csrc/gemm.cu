@@ -45,6 +45,7 @@
 // returns.
 #include <cstdint>
 
+#include "e4m3.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -78,7 +79,9 @@ constexpr int ALIGN_PAD = 1024;            // 128-byte-swizzled tiles need 1024-
 
 // Shared-memory layout per CTA. PAIR: a CTA holds its A tile and half of the W tile.
 // RS: the B operand has a scale per row and K block (the 1d1d GEMM) instead of per 128x128 block.
-template <bool GROUPED, bool PAIR, bool RS>
+// SW: the SwiGLU + re-quantizing epilogue, which exchanges row maxima between the two warps that
+// share a 1x128 output tile (two tile-parity buffers x two halves x 128 rows of FP32).
+template <bool GROUPED, bool PAIR, bool RS, bool SW = false>
 struct Layout {
     static constexpr int SLOT = RS ? SCALE_SLOT_BYTES_ROWS : SCALE_SLOT_BYTES_BLOCK;
     static constexpr int CL = PAIR ? 2 : 1;              // CTAs per cluster
@@ -89,9 +92,11 @@ struct Layout {
     static constexpr int B_OFF = STAGES * A_BYTES;
     static constexpr int STG_OFF = STAGES * STAGE;
     static constexpr int SCL_OFF = STG_OFF + STG_BYTES;
-    static constexpr int BAR_OFF = SCL_OFF + SCALE_SLOTS * SLOT;
-    // full[S], empty[S], tfull[2], tempty[2], drain, sfull[SCALE_SLOTS], sempty[SCALE_SLOTS]
-    static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * SCALE_SLOTS;
+    static constexpr int XCH_OFF = SCL_OFF + SCALE_SLOTS * SLOT;
+    static constexpr int BAR_OFF = XCH_OFF + (SW ? 2 * 2 * 128 * 4 : 0);
+    // full[S], empty[S], tfull[2], tempty[2], drain, sfull[SCALE_SLOTS], sempty[SCALE_SLOTS],
+    // SW: xch[4] (one per TMEM lane quarter)
+    static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * SCALE_SLOTS + (SW ? 4 : 0);
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int GROUP_OFF = MISC_OFF + 16;
     static_assert(A_BYTES % 1024 == 0 && B_PART % 1024 == 0, "tiles keep 1024-byte alignment");
@@ -185,6 +190,19 @@ __device__ __forceinline__ float ld_shared_f32(uint32_t addr)
     return v;
 }
 
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v)
+{
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// SiLU in FP32, g / (1 + e^-g), with the fast exponential and division intrinsics (a few FP32
+// ulps; the accurate forms made the fused epilogue's tail 20% of the GEMM). For g below about
+// -88 the exponential overflows to +inf and the result is -0.
+__device__ __forceinline__ float silu(float g)
+{
+    return __fdividef(g, 1.0f + __expf(-g));
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, const uint4& v)
 {
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
@@ -209,12 +227,13 @@ __device__ __forceinline__ void st_v4(void* p, uint32_t a, uint32_t b, uint32_t 
                  : "memory");
 }
 
-template <bool GROUPED, bool OUT_F32, bool PAIR, bool RS>
+template <bool GROUPED, bool OUT_F32, bool PAIR, bool RS, bool SW>
 __global__ void __launch_bounds__(THREADS, 1)
 fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                             const __grid_constant__ CUtensorMap map_b, const GemmArgs p)
 {
-    using L = Layout<GROUPED, PAIR, RS>;
+    using L = Layout<GROUPED, PAIR, RS, SW>;
+    static_assert(!SW || (GROUPED && !PAIR && !RS && !OUT_F32), "SwiGLU epilogue: grouped only");
     constexpr int STAGES = L::STAGES;
     constexpr int CL = L::CL;
     extern __shared__ uint8_t smem_raw[];
@@ -232,6 +251,7 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     const uint32_t drain_bar = tempty0 + 16;
     const uint32_t sfull0 = drain_bar + 8;
     const uint32_t sempty0 = sfull0 + 8 * SCALE_SLOTS;
+    const uint32_t xch0 = sempty0 + 8 * SCALE_SLOTS;   // SW only
     const uint32_t scl0 = base + L::SCL_OFF;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
     const uint32_t abort_addr = base + L::MISC_OFF + 4;   // shared word: a role gave up
@@ -260,6 +280,9 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
         for (int i = 0; i < SCALE_SLOTS; i++) {
             mbar_init(sfull0 + 8 * i, 32);              // one cp.async completion per loader lane
             mbar_init(sempty0 + 8 * i, NUM_EPI_WARPS);
+        }
+        if constexpr (SW) {
+            for (int q = 0; q < 4; q++) mbar_init(xch0 + 8 * q, 2);   // the two warps of a quad
         }
         st_shared_volatile_u32(abort_addr, 0u);
         fence_mbar_init();
@@ -495,13 +518,15 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
         regs_inc<REGS_EPILOGUE>();
         // ---------------------------------------------------------------- epilogue
         const int quad = warp & 3;                   // TMEM lanes 32*quad .. 32*quad + 31
-        const int half = (warp - EPI_WARP0) >> 2;    // columns 128*half .. 128*half + 127
+        const int half = (warp - EPI_WARP0) >> 2;    // columns 128*half .. 128*half + 127 (SW:
+                                                     // gate 64*half.. + 63 and up 128 + 64*half..)
         const int r = quad * 32 + lane;              // row within the tile
         const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
         uint32_t j = 0;
         uint64_t acc[64];   // 128 FP32 accumulators as packed pairs (columns 2i, 2i + 1)
+        uint32_t tile_n = 0;   // tiles finished by this CTA (SW: parity of the exchange buffers)
 
-        for (int t = cluster_id; t < num_tiles; t += num_clusters) {
+        for (int t = cluster_id; t < num_tiles; t += num_clusters, tile_n++) {
             const int ncol0 =
                 decode_tile<GROUPED, CL>(t, p, s_tstart, s_off, static_cast<int>(crank)).n0 +
                 half * 128;
@@ -523,9 +548,12 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                 // Block-scaled B: one product s_a[row] * s_w[block] per K block. RS: s_a[row]
                 // here, times s_b[column] per column pair below (B-row scales stay in the slot
                 // until the promotion is done).
+                // SW: the gate half of the tile (W block 2 nt) and the up half (block 2 nt + 1).
                 const float sc = RS ? ld_shared_f32(sl + r * 4)
                                     : __fmul_rn(ld_shared_f32(sl + r * 4),
-                                                ld_shared_f32(sl + 512 + half * 4));
+                                                ld_shared_f32(sl + 512 + (SW ? 0 : half) * 4));
+                const float sc_up =
+                    SW ? __fmul_rn(ld_shared_f32(sl + r * 4), ld_shared_f32(sl + 516)) : sc;
                 const uint32_t sb = sl + 512 + half * 128 * 4;   // RS: s_b of this half's columns
                 if constexpr (!RS) {
                     __syncwarp();
@@ -543,8 +571,9 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                 tc_fence_after();
                 // Four 32-column chunks; the TMEM load of chunk c+1 is in flight while chunk c
                 // is promoted (two register buffers of 16 packed pairs).
-                const uint32_t taddr = tmem_base + t_lane + b * BN + half * 128;
+                const uint32_t taddr = tmem_base + t_lane + b * BN + half * (SW ? 64 : 128);
                 const uint64_t sc2 = f32x2_splat(sc);
+                const uint64_t sc2b = f32x2_splat(sc_up);        // SW: the up columns
                 if constexpr (RS) {
                     // Per-column scales, eight 16-column chunks: acc = fma(P * s_b[n], s_a[m], acc)
                     // (the product P * s_b depends on the TMEM data, so it is formed only when
@@ -566,6 +595,28 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                         for (int i = 0; i < 8; i++)
                             ffma2(acc[8 * (c + 1) + i],
                                   fmul2(u1[i], ld_shared_u64(sb + 64 * (c + 1) + 8 * i)), sc2);
+                    }
+                } else if constexpr (SW) {
+                    // gate columns 64 half .. + 63 into acc[0..31] (scale s_a * s_w[gate block]),
+                    // up columns 128 + 64 half .. + 63 into acc[32..63] (s_a * s_w[up block]);
+                    // 16-column chunks leave registers for the SwiGLU tail below
+                    uint64_t u0[8], u1[8];
+                    tmem_ld_16cols(taddr, u0);
+#pragma unroll
+                    for (int c = 0; c < 8; c += 2) {
+                        const uint32_t col1 = (c + 1 < 4) ? 16 * (c + 1) : 128 + 16 * (c + 1 - 4);
+                        tmem_wait_ld(u0);
+                        tmem_ld_16cols(taddr + col1, u1);
+#pragma unroll
+                        for (int i = 0; i < 8; i++) ffma2(acc[8 * c + i], u0[i], c < 4 ? sc2 : sc2b);
+                        tmem_wait_ld(u1);
+                        if (c + 2 < 8) {
+                            const uint32_t col2 = (c + 2 < 4) ? 16 * (c + 2) : 128 + 16 * (c + 2 - 4);
+                            tmem_ld_16cols(taddr + col2, u0);
+                        }
+#pragma unroll
+                        for (int i = 0; i < 8; i++)
+                            ffma2(acc[8 * (c + 1) + i], u1[i], c + 1 < 4 ? sc2 : sc2b);
                     }
                 } else {
                     uint64_t v0[16], v1[16];
@@ -596,6 +647,67 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     mbar_arrive(tempty0 + 8 * b);
             }
             if (!ok) break;
+
+            if constexpr (SW) {
+                // h = silu(g) * u for this thread's 64 channels (g in acc[0..31], u in
+                // acc[32..63]), then the 1x128 tile of h: its amax combines this warp's 64
+                // channels with the partner warp's (same rows, other half), exchanged through
+                // shared memory; then scale, codes, and a staged store of 64 codes per row.
+                float amax = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 32; i++) {
+                    const float h0 = __fmul_rn(silu(f32x2_lo(acc[i])), f32x2_lo(acc[32 + i]));
+                    const float h1 = __fmul_rn(silu(f32x2_hi(acc[i])), f32x2_hi(acc[32 + i]));
+                    acc[i] = f32x2_pack(h0, h1);
+                    amax = fmaxf(amax, fmaxf(fabsf(h0), fabsf(h1)));
+                }
+                const uint32_t xbuf = base + L::XCH_OFF + (tile_n & 1u) * 1024;
+                st_shared_f32(xbuf + half * 512 + r * 4, amax);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(xch0 + 8 * quad);
+                const bool xok = mbar_wait(xch0 + 8 * quad, tile_n & 1u, abort_addr, budget);
+                if (!__all_sync(0xffffffffu, xok)) {
+                    if (lane == 0) raise_error(p.err, abort_addr, DEV_TIMEOUT_EPILOGUE);
+                    break;
+                }
+                amax = fmaxf(amax, ld_shared_f32(xbuf + (half ^ 1) * 512 + r * 4));
+                const TileScale tsc = tile_scale(amax);
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; i++) {
+                    const uint32_t lo = cvt_e4m3x2(tile_scaled(f32x2_lo(acc[2 * i]), tsc),
+                                                   tile_scaled(f32x2_hi(acc[2 * i]), tsc));
+                    const uint32_t hi = cvt_e4m3x2(tile_scaled(f32x2_lo(acc[2 * i + 1]), tsc),
+                                                   tile_scaled(f32x2_hi(acc[2 * i + 1]), tsc));
+                    w[i] = tsc.zero ? 0u : (lo | (hi << 16));
+                }
+                const TileInfo ts =
+                    decode_tile<GROUPED, CL>(t, p, s_tstart, s_off, static_cast<int>(crank));
+                const int64_t grow_own = ts.row0 + r;
+                const int ob = ts.n0 / BN;                       // 1x128 output tile index
+                if (half == 0 && grow_own < ts.row_end)
+                    p.h_s[static_cast<int64_t>(ob) * p.rows + grow_own] = tsc.s;
+                // 32 rows x 64 code bytes of this warp, staged as in the store below
+                const uint32_t stg = base + L::STG_OFF + (warp - EPI_WARP0) * STG_WARP_BYTES;
+#pragma unroll
+                for (int jc = 0; jc < 4; jc++)
+                    st_shared_v4(stg + lane * 64 + (((jc + (lane >> 1)) & 3) * 16),
+                                 make_uint4(w[4 * jc], w[4 * jc + 1], w[4 * jc + 2], w[4 * jc + 3]));
+                __syncwarp();
+                const int ch = lane & 3;
+                const int64_t gcol = static_cast<int64_t>(ob) * 128 + half * 64 + ch * 16;
+                const int64_t wrow0 = ts.row0 + quad * 32;
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    const int rr = i * 8 + (lane >> 2);
+                    const uint4 v = ld_shared_v4(stg + rr * 64 + (((ch + (rr >> 1)) & 3) * 16));
+                    const int64_t grow = wrow0 + rr;
+                    if (grow < ts.row_end)
+                        st_v4(static_cast<uint8_t*>(p.c) + grow * p.ldc + gcol, v.x, v.y, v.z, v.w);
+                }
+                __syncwarp();
+                continue;
+            }
 
             // Store: stage this warp's 32 rows x 64 B at a time in shared memory, chunk j (16 B)
             // of row r at position (j + r/2) % 4, which keeps both the row-wise writes and the
@@ -656,13 +768,16 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     if constexpr (PAIR) cluster_sync();   // no CTA leaves while its peer still deallocates
 }
 
-template <bool GROUPED, bool OUT_F32, bool PAIR, bool RS>
+template <bool GROUPED, bool OUT_F32, bool PAIR, bool RS, bool SW = false>
 cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& args,
                        int max_ctas, cudaStream_t stream)
 {
     constexpr int CL = PAIR ? 2 : 1;
-    auto kern = fp8_blockscaled_gemm_kernel<GROUPED, OUT_F32, PAIR, RS>;
-    const size_t smem = gemm_smem_bytes(GROUPED, RS, args.G);
+    auto kern = fp8_blockscaled_gemm_kernel<GROUPED, OUT_F32, PAIR, RS, SW>;
+    const size_t smem = gemm_smem_bytes(
+        SW ? GemmKind::GROUPED_SWIGLU
+           : (RS ? GemmKind::ROW_SCALED : (GROUPED ? GemmKind::GROUPED : GemmKind::DENSE)),
+        args.G);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -698,15 +813,22 @@ cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const GemmA
 
 }  // namespace
 
-size_t gemm_smem_bytes(bool grouped, bool row_scaled_b, int G)
+size_t gemm_smem_bytes(GemmKind kind, int G)
 {
     constexpr bool DENSE_PAIR = GEMM_DENSE_CLUSTER == 2;
-    if (row_scaled_b)
+    const size_t group_table = 2 * static_cast<size_t>(G + 1) * sizeof(int);
+    switch (kind) {
+    case GemmKind::ROW_SCALED:
         return static_cast<size_t>(Layout<false, DENSE_PAIR, true>::GROUP_OFF) + ALIGN_PAD;
-    if (!grouped)
+    case GemmKind::GROUPED:
+        return static_cast<size_t>(Layout<true, false, false>::GROUP_OFF) + ALIGN_PAD + group_table;
+    case GemmKind::GROUPED_SWIGLU:
+        return static_cast<size_t>(Layout<true, false, false, true>::GROUP_OFF) + ALIGN_PAD +
+               group_table;
+    case GemmKind::DENSE:
+    default:
         return static_cast<size_t>(Layout<false, DENSE_PAIR, false>::GROUP_OFF) + ALIGN_PAD;
-    return static_cast<size_t>(Layout<true, false, false>::GROUP_OFF) + ALIGN_PAD +
-           2 * static_cast<size_t>(G + 1) * sizeof(int);
+    }
 }
 
 int gemm_cluster_size(bool grouped) { return grouped ? 1 : GEMM_DENSE_CLUSTER; }
@@ -719,6 +841,8 @@ cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, cons
     case GemmKind::GROUPED:
         return out_f32 ? launch_one<true, true, false, false>(map_a, map_b, args, max_ctas, stream)
                        : launch_one<true, false, false, false>(map_a, map_b, args, max_ctas, stream);
+    case GemmKind::GROUPED_SWIGLU:
+        return launch_one<true, false, false, false, true>(map_a, map_b, args, max_ctas, stream);
     case GemmKind::ROW_SCALED:
         return out_f32 ? launch_one<false, true, DP, true>(map_a, map_b, args, max_ctas, stream)
                        : launch_one<false, false, DP, true>(map_a, map_b, args, max_ctas, stream);

@@ -43,6 +43,7 @@ struct GemmArgs {
     int MT;                   // dense: ceil(M / 128)
     int num_tiles;            // dense: work items = ceil(MT / cluster) * NT (grouped: on device)
     const int32_t* offsets;   // grouped: [G+1] on the device
+    float* h_s;               // GROUPED_SWIGLU: output scales [N/256][rows] (codes go to c)
     int G;
     int* err;                 // device error word
     long long budget;         // spin-wait budget in SM clock cycles
@@ -66,11 +67,13 @@ int take_fault_skip_release();
 
 // DENSE: per-128x128-block B scales; GROUPED: the same per expert; ROW_SCALED: a scale per B
 // row and K block (the 1d1d weight-gradient GEMM), dense only.
-enum class GemmKind { DENSE, GROUPED, ROW_SCALED };
+// GROUPED_SWIGLU: grouped, gate/up rows interleaved per 128, epilogue silu(gate) * up re-quantized
+// to E4M3 with 1x128 scales.
+enum class GemmKind { DENSE, GROUPED, ROW_SCALED, GROUPED_SWIGLU };
 cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args,
                         GemmKind kind, bool out_f32, int max_ctas, cudaStream_t stream);
 int gemm_cluster_size(bool grouped);
-size_t gemm_smem_bytes(bool grouped, bool row_scaled_b, int G);
+size_t gemm_smem_bytes(GemmKind kind, int G);
 
 // ------------------------------------------------------------------------------------
 // Host-side helpers of the C ABI (api.cu)

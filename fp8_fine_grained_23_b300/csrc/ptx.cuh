@@ -402,6 +402,12 @@ __device__ __forceinline__ float f32x2_hi(uint64_t v)
     return __uint_as_float(static_cast<uint32_t>(v >> 32));
 }
 
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi)
+{
+    return static_cast<uint64_t>(__float_as_uint(lo)) |
+           (static_cast<uint64_t>(__float_as_uint(hi)) << 32);
+}
+
 // Shared-memory matrix descriptor for a K-major operand tile whose rows are 128 bytes long and
 // laid out with the 128-byte swizzle (what a TMA load with CU_TENSOR_MAP_SWIZZLE_128B and a
 // 128-byte inner box writes): 8-row groups 1024 bytes apart. The tile must be 1024-aligned;

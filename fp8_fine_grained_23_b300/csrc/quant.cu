@@ -13,39 +13,13 @@
 // rounded and subnormals are kept, which the bit-exact contract depends on.
 #include <cstdint>
 
+#include "e4m3.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace fp8bs {
 
 namespace {
-
-struct TileScale {
-    float s;     // dequantization scale
-    float r;     // quantization multiplier
-    bool tiny;   // amax < 2^-64: r formed from amax * 2^64 (exact), values scaled by 2^64
-    bool zero;   // amax == 0: scale 1, codes 0x00
-};
-
-__device__ __forceinline__ TileScale tile_scale(float amax)
-{
-    TileScale t;
-    t.zero = (amax == 0.0f);
-    t.tiny = !t.zero && (amax < 0x1p-64f);
-    const float den = t.tiny ? __fmul_rn(amax, 0x1p64f) : amax;
-    t.s = t.zero ? 1.0f : __fdiv_rn(amax, 448.0f);
-    t.r = t.zero ? 0.0f : __fdiv_rn(448.0f, den);
-    return t;
-}
-
-// Two FP32 values to two E4M3 codes, saturating round-to-nearest-even; `lo` lands in the low
-// byte of the result.
-__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi)
-{
-    uint16_t r;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    return r;
-}
 
 __device__ __forceinline__ void unpack_bf16x8(const uint4& v, float (&f)[8])
 {

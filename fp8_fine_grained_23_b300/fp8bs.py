@@ -32,6 +32,8 @@ lib.fp8_blockscaled_grouped_gemm.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i6
 lib.fp8_quant_act_128x1.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p, _p]
 lib.fp8_quant_weight_128x128_t.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p, _p]
 lib.fp8_blockscaled_gemm_1d1d.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, _p, _i64, _int, _p]
+lib.fp8_blockscaled_grouped_gemm_swiglu_quant.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64,
+                                                         _i64, _p, _i64, _p, _p]
 lib.fp8bs_status_string.argtypes = [_int]
 lib.fp8bs_status_string.restype = ctypes.c_char_p
 lib.fp8bs_last_error.argtypes = [_p]
@@ -39,7 +41,8 @@ lib.fp8bs_debug_skip_release.argtypes = [_int]
 for _f in (lib.fp8_quant_act_1x128, lib.fp8_quant_weight_128x128, lib.fp8_blockscaled_gemm,
            lib.fp8_blockscaled_gemm_noalloc, lib.fp8_blockscaled_grouped_gemm,
            lib.fp8bs_last_error, lib.fp8bs_debug_skip_release, lib.fp8_quant_act_128x1,
-           lib.fp8_quant_weight_128x128_t, lib.fp8_blockscaled_gemm_1d1d):
+           lib.fp8_quant_weight_128x128_t, lib.fp8_blockscaled_gemm_1d1d,
+           lib.fp8_blockscaled_grouped_gemm_swiglu_quant):
     _f.restype = _int
 
 FP8BS_OK = 0
@@ -228,6 +231,31 @@ def fp8_blockscaled_grouped_gemm(a_q: torch.Tensor, a_s: torch.Tensor, w_q: torc
                                             out.data_ptr(), ldc, _out_code(out.dtype),
                                             _stream(stream)))
     return out
+
+
+def fp8_blockscaled_grouped_gemm_swiglu_quant(a_q: torch.Tensor, a_s: torch.Tensor,
+                                              w_q: torch.Tensor, w_s: torch.Tensor,
+                                              group_offsets: torch.Tensor,
+                                              h_q: torch.Tensor | None = None,
+                                              h_s: torch.Tensor | None = None, stream=None):
+    """Grouped gate/up GEMM (w_q [G][N2][K], gate and up rows interleaved per 128) with the
+    SwiGLU h = silu(gate) * up re-quantized in 1x128 tiles: codes h_q [R][N2/2], scales
+    h_s [N2/256][R]."""
+    R, K = a_q.shape
+    G, N2 = w_q.shape[0], w_q.shape[1]
+    if group_offsets.dtype != torch.int32 or group_offsets.numel() != G + 1:
+        raise ValueError("group_offsets must be int32 with G + 1 entries")
+    if h_q is None:
+        h_q = torch.empty(R, N2 // 2, dtype=torch.uint8, device=a_q.device)
+    if h_s is None:
+        h_s = torch.empty(N2 // 256, R, dtype=torch.float32, device=a_q.device)
+    _, ldh = _rows_ld(h_q, "h_q")
+    _check("fp8_blockscaled_grouped_gemm_swiglu_quant",
+           lib.fp8_blockscaled_grouped_gemm_swiglu_quant(
+               a_q.data_ptr(), a_s.data_ptr(), w_q.data_ptr(), w_s.data_ptr(),
+               group_offsets.data_ptr(), G, R, N2, K, h_q.data_ptr(), ldh, h_s.data_ptr(),
+               _stream(stream)))
+    return h_q, h_s
 
 
 def fp8bs_last_error(stream=None) -> int:

@@ -129,6 +129,34 @@ int fp8_blockscaled_grouped_gemm(const uint8_t *a_q, const float *a_s,
                                  fp8bs_stream_t stream);
 
 /*
+ * Grouped GEMM with a fused SwiGLU and 1x128 re-quantization of its output, for the expert FFN
+ * (gate and up projections, then the down projection). The pages keep GEMM inputs in FP8,
+ * accumulate in higher precision and convert back to FP8 for the next computation (szhzxw.cn
+ * 一.2.c; [codingmall] "Định lượng trực tuyến": scales from the current tile maximum). The
+ * activation between the two expert GEMMs is not on the pages; this call takes SwiGLU,
+ * h = silu(gate) * up, DeepSeek-V3's expert FFN activation (a reading).
+ *   w_q    E4M3 [G][N2][K] with gate and up rows interleaved in blocks of 128: rows
+ *          [256 j, 256 j + 128) are the gate rows of channels [128 j, 128 j + 128) and rows
+ *          [256 j + 128, 256 j + 256) their up rows; w_s FP32 [G][N2/128][K/128] as usual.
+ *   a_q, a_s, group_offsets, G, R, K  as for fp8_blockscaled_grouped_gemm.
+ *   h_q    E4M3 codes [R][ldh] of h, I = N2/2 channels per row (the A operand of the down GEMM)
+ *   h_s    FP32 [I/128][R]: one scale per row and 128 channels (the 1x128 activation layout)
+ * Per row r of group g: gate[c], up[c] = the block-scaled GEMM (FP32 accumulation as in
+ * fp8_blockscaled_gemm) against expert g's gate/up rows of channel c; h[c] = fl(silu(gate[c]) *
+ * up[c]) with silu(x) = x / (1 + e^-x) in FP32 from the fast exponential and division
+ * intrinsics (__expf, __fdividef: a few ulps); then each 1x128 tile of h is quantized
+ * exactly as fp8_quant_act_1x128 quantizes a tile (s = amax/448, codes E4M3(h * 448/amax)).
+ * Requires N2 > 0, N2 % 256 == 0, ldh >= N2/2, ldh % 16 == 0, h_q 16-byte and h_s 4-byte
+ * aligned, plus the grouped call's rules for the inputs. Rows outside every group are not
+ * written.
+ */
+int fp8_blockscaled_grouped_gemm_swiglu_quant(const uint8_t *a_q, const float *a_s,
+                                              const uint8_t *w_q, const float *w_s,
+                                              const int32_t *group_offsets, int64_t G, int64_t R,
+                                              int64_t N2, int64_t K, uint8_t *h_q, int64_t ldh,
+                                              float *h_s, fp8bs_stream_t stream);
+
+/*
  * Backward pass. The pages use the same E4M3 format in the backward pass as in the forward
  * pass ([codingmall] "Định dạng E4M3 hợp nhất"; [dtcms] 三.2) and name no backward tile shapes.
  * Reading: a block-scaled contraction needs one scale per 128-long block of the contracted

@@ -139,3 +139,14 @@ def oracle_points_1d1d(aq, a_s, bq, b_s, pm, pn):
             lambda i: O.gemm_1d1d_points(aq, a_s, bq, b_s, pm[cuts[i]:cuts[i + 1]],
                                          pn[cuts[i]:cuts[i + 1]]), range(THREADS)))
     return np.concatenate([p[0] for p in parts]), np.concatenate([p[1] for p in parts])
+
+
+def oracle_grouped_swiglu_rows(aq, a_s, wq, w_s, offsets, rows):
+    """O.grouped_swiglu_rows split over host threads by rows."""
+    rows = np.asarray(rows, np.int64)
+    cuts = np.linspace(0, rows.size, min(THREADS, rows.size) + 1).astype(int)
+    with ThreadPoolExecutor(THREADS) as ex:
+        parts = list(ex.map(lambda i: O.grouped_swiglu_rows(aq, a_s, wq, w_s, offsets,
+                                                            rows[cuts[i]:cuts[i + 1]]),
+                            range(len(cuts) - 1)))
+    return tuple(np.concatenate([p[k] for p in parts]) for k in range(5))

@@ -28,7 +28,8 @@ def test_header_declares_the_hot_path_calls():
     names = declared_functions()
     for n in ("fp8_quant_act_1x128", "fp8_quant_weight_128x128", "fp8_blockscaled_gemm",
               "fp8_blockscaled_grouped_gemm", "fp8bs_status_string", "fp8bs_last_error",
-              "fp8_quant_act_128x1", "fp8_quant_weight_128x128_t", "fp8_blockscaled_gemm_1d1d"):
+              "fp8_quant_act_128x1", "fp8_quant_weight_128x128_t", "fp8_blockscaled_gemm_1d1d",
+              "fp8_blockscaled_grouped_gemm_swiglu_quant"):
         assert n in names
 
 
@@ -119,6 +120,19 @@ def test_transpose_quant_argument_checks(F, fn, args, expect):
 def test_gemm_1d1d_argument_checks(F, mnk, ldc, dt, expect):
     M, N, K = mnk
     assert F.lib.fp8_blockscaled_gemm_1d1d(P16, P4, P16, P4, M, N, K, P16, ldc, dt, None) == expect
+
+
+def test_swiglu_quant_argument_checks(F):
+    f = F.lib.fp8_blockscaled_grouped_gemm_swiglu_quant
+    ok = (P16, P4, P16, P4, P4, 2, 8, 512, 128, P16, 256, P4)
+    assert f(*ok[:6], 0, *ok[7:], None) == 0                                      # R == 0
+    assert f(*ok[:5], 0, *ok[6:], None) == -1                                     # G < 1
+    assert f(*ok[:7], 384, *ok[8:], None) == -1                                   # N2 % 256
+    assert f(*ok[:10], 128, ok[11], None) == -1                                   # ldh < N2/2
+    assert f(*ok[:10], 264, ok[11], None) == -2                                   # ldh % 16
+    assert f(*ok[:9], P16 + 4, *ok[10:], None) == -2                              # h_q alignment
+    assert f(*ok[:11], P4 + 1, None) == -2                                        # h_s alignment
+    assert f(*ok[:11], None, None) == -1                                          # no h_s
 
 
 def test_debug_hook_rejects_negative_index(F):
