@@ -190,6 +190,22 @@ def moe_routing(shape: MoEShape = MOE) -> tuple[np.ndarray, np.ndarray]:
     return offsets, token_of_row[order]
 
 
+def moe_row_of_token(token_of_row: np.ndarray, tokens: int, topk: int) -> np.ndarray:
+    """Inverse of the routing's row order: int32 [tokens][topk], the sorted rows that hold each
+    token, in increasing row (= expert) order."""
+    order = np.argsort(token_of_row, kind="stable")        # rows grouped by token, rows ascending
+    return order.astype(np.int32).reshape(tokens, topk)
+
+
+def moe_gate_weights(shape: MoEShape = MOE) -> np.ndarray:
+    """Routing weights float32 [tokens][topk]: a seeded softmax over each token's selected
+    experts (positive, summing to 1 per token), in the order of moe_row_of_token."""
+    rng = np.random.default_rng(shape.seed + 2)
+    logits = rng.standard_normal((shape.tokens, shape.topk))
+    e = np.exp(logits - logits.max(axis=1, keepdims=True))
+    return (e / e.sum(axis=1, keepdims=True)).astype(np.float32)
+
+
 def synthetic_offsets(counts) -> np.ndarray:
     """Group offsets from explicit per-group row counts (edge-case tests)."""
     counts = np.asarray(counts, np.int64)

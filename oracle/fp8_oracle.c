@@ -62,6 +62,17 @@ static float bf16_bits_to_float(uint16_t h)
     return f;
 }
 
+/* Round a finite binary32 to BF16, nearest with ties to even: add 0x7FFF plus the kept part's
+ * lowest bit to the bit pattern and truncate (a carry into the exponent is the correct
+ * rounding up). Non-finite values are outside the contract. */
+static uint16_t float_to_bf16_rne(float f)
+{
+    uint32_t b;
+    memcpy(&b, &f, 4);
+    b += 0x7FFFu + ((b >> 16) & 1u);
+    return (uint16_t)(b >> 16);
+}
+
 /* Value of one E4M3FN code: sign s, biased exponent e (bias 7), mantissa m.
  * e == 0 is subnormal: m * 2^-9. Otherwise (1 + m/8) * 2^(e-7). S.1111.111 is NaN. */
 double orc_e4m3_decode(uint8_t code)
@@ -431,6 +442,40 @@ void orc_swiglu_f64(const double *g, const double *u, int64_t n, double *h)
 {
     for (int64_t i = 0; i < n; i++)
         h[i] = g[i] / (1.0 + exp(-g[i])) * u[i];
+}
+
+/* MoE dispatch, token side ([MoE]: each token routed to 8 of 256 experts; the expert GEMMs run on
+ * rows sorted by expert). Permute: row r of the sorted operand is token tok[r]'s row, codes and
+ * 1x128 scales alike: qp[r][k] = q[tok[r]][k], sp[kb][r] = s[kb][tok[r]].
+ * q [T][ldq], s [K/128][T]; qp [R][ldqp], sp [K/128][R]. */
+void orc_moe_permute(const uint8_t *q, int64_t ldq, const float *s, int64_t T,
+                     const int32_t *tok, int64_t R, int64_t K, uint8_t *qp, int64_t ldqp, float *sp)
+{
+    int64_t KB = K / 128;
+    for (int64_t r = 0; r < R; r++) {
+        int64_t t = tok[r];
+        for (int64_t k = 0; k < K; k++)
+            qp[r * ldqp + k] = q[t * ldq + k];
+        for (int64_t kb = 0; kb < KB; kb++)
+            sp[kb * R + r] = s[kb * T + t];
+    }
+}
+
+/* MoE combine: token t's output is the routing-weighted sum of its expert rows,
+ * out[t][n] = sum_j w[t][j] * y[row[t][j]][n], summed in FP32 as acc = fmaf(w, y, acc) for
+ * j = 0 .. topk-1 in order from acc = 0, then rounded to BF16 (nearest, ties to even).
+ * y BF16 bits [R][ldy]; row int32 [T][topk]; w FP32 [T][topk]; out BF16 bits [T][ldo]. */
+void orc_moe_combine(const uint16_t *y, int64_t ldy, const int32_t *row, const float *w,
+                     int64_t T, int64_t topk, int64_t N, uint16_t *out, int64_t ldo)
+{
+    for (int64_t t = 0; t < T; t++)
+        for (int64_t n = 0; n < N; n++) {
+            float acc = 0.0f;
+            for (int64_t j = 0; j < topk; j++)
+                acc = fmaf(w[t * topk + j], bf16_bits_to_float(y[(int64_t)row[t * topk + j] * ldy + n]),
+                           acc);
+            out[t * ldo + n] = float_to_bf16_rne(acc);
+        }
 }
 
 /* Unquantized FP64 product of the BF16 inputs, C[m][n] = sum_k x[m,k] * w[n,k]; used only to

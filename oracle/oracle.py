@@ -68,11 +68,14 @@ def lib() -> ctypes.CDLL:
             L.orc_gemm_1d1d_points.argtypes = [_p, _i64, _p, _p, _i64, _p, _i64, _i64, _i64,
                                                _i64, _p, _p, _p, _p, _p]
             L.orc_swiglu_f64.argtypes = [_p, _p, _i64, _p]
+            L.orc_moe_permute.argtypes = [_p, _i64, _p, _i64, _p, _i64, _i64, _p, _i64, _p]
+            L.orc_moe_combine.argtypes = [_p, _i64, _p, _p, _i64, _i64, _i64, _p, _i64]
             for f in (L.orc_e4m3_encode_array, L.orc_e4m3_decode_array, L.orc_quant_act_1x128,
                       L.orc_quant_weight_128x128, L.orc_gemm_points, L.orc_gemm_f64,
                       L.orc_grouped_gemm_points, L.orc_gemm_unquantized_f64,
                       L.orc_quant_act_128x1, L.orc_quant_weight_128x128_t,
-                      L.orc_gemm_1d1d_points, L.orc_swiglu_f64):
+                      L.orc_gemm_1d1d_points, L.orc_swiglu_f64, L.orc_moe_permute,
+                      L.orc_moe_combine):
                 f.restype = None
             _lib = L
         return _lib
@@ -263,6 +266,29 @@ def grouped_swiglu_rows(aq, a_s, wq, w_s, offsets, rows):
     shape = (rows.size, I)
     g, gabs, u, uabs = (x.reshape(shape) for x in (g, gabs, u, uabs))
     return swiglu_f64(g, u), g, gabs, u, uabs
+
+
+def moe_permute(q, s, tok) -> tuple[np.ndarray, np.ndarray]:
+    """Rows of (codes q [T][K], scales s [K/128][T]) gathered in the order tok [R]:
+    (qp [R][K], sp [K/128][R])."""
+    q, s, tok = _c(q, np.uint8), _c(s, np.float32), _c(tok, np.int32)
+    T, K = q.shape
+    R = tok.size
+    qp = np.empty((R, K), np.uint8)
+    sp = np.empty((K // 128, R), np.float32)
+    lib().orc_moe_permute(_ptr(q), K, _ptr(s), T, _ptr(tok), R, K, _ptr(qp), K, _ptr(sp))
+    return qp, sp
+
+
+def moe_combine(y_bits, row, w) -> np.ndarray:
+    """out[t] = sum_j w[t][j] * y[row[t][j]] (FP32 fma chain in j order, then BF16 RNE).
+    y_bits uint16 [R][N]; row int32 [T][topk]; w float32 [T][topk]. Returns uint16 [T][N]."""
+    y, row, w = _c(y_bits, np.uint16), _c(row, np.int32), _c(w, np.float32)
+    R, N = y.shape
+    T, topk = row.shape
+    out = np.empty((T, N), np.uint16)
+    lib().orc_moe_combine(_ptr(y), N, _ptr(row), _ptr(w), T, topk, N, _ptr(out), N)
+    return out
 
 
 def gemm_unquantized_f64(x_bits, w_bits) -> np.ndarray:
