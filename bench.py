@@ -487,6 +487,29 @@ def run_extras(F, dev, peaks, fp8_peak):
         "steps": "gate/up GEMM + SwiGLU + 1x128 re-quantization, then the down GEMM on h"}
     del ops, aq, a_s, wq, w_s, dq, ds_, dwq, dws, hq, hs, y
     torch.cuda.empty_cache()
+    # token-side dispatch: permute the quantized tokens into expert order; combine the expert
+    # outputs back per token with the routing weights
+    T, Kh = shape.tokens, shape.hidden
+    xq, xs = F.fp8_quant_act_1x128(WL.moe_tokens(shape, dev))
+    tok = torch.from_numpy(token_of_row.astype(np.int32)).to(dev)
+    qp = torch.empty(R, Kh, dtype=torch.uint8, device=dev)
+    sp = torch.empty(Kh // 128, R, dtype=torch.float32, device=dev)
+    ms = _timed(lambda: F.fp8_moe_permute(xq, xs, tok, qp, sp), dev)
+    pbytes = 2 * R * Kh + 2 * sp.numel() * 4 + tok.numel() * 4
+    moe["permute"] = {"us": round(ms * 1e3, 2), "GB/s": round(pbytes / (ms * 1e-3) / 1e9, 1),
+                      "frac_hbm": round(pbytes / (ms * 1e-3) / 1e9 / hbm, 4),
+                      "rows": R, "K": Kh}
+    rows = torch.from_numpy(WL.moe_row_of_token(token_of_row, T, shape.topk)).to(dev)
+    gw = torch.from_numpy(WL.moe_gate_weights(shape)).to(dev)
+    yv = WL.activations(R, Kh, WL.generator(shape.seed + 3, dev), dev)   # expert outputs
+    outv = torch.empty(T, Kh, dtype=torch.bfloat16, device=dev)
+    ms = _timed(lambda: F.fp8_moe_combine(yv, rows, gw, outv), dev)
+    cbytes = 2 * R * Kh + 2 * T * Kh + rows.numel() * 8
+    moe["combine"] = {"us": round(ms * 1e3, 2), "GB/s": round(cbytes / (ms * 1e-3) / 1e9, 1),
+                      "frac_hbm": round(cbytes / (ms * 1e-3) / 1e9 / hbm, 4),
+                      "tokens": T, "topk": shape.topk, "N": Kh}
+    del xq, xs, tok, qp, sp, rows, gw, yv, outv
+    torch.cuda.empty_cache()
     out["moe_grouped_gemm"] = moe
     out["backward"] = run_backward(F, dev, hbm, fp8_peak)
     if F.fp8bs_last_error() != F.FP8BS_OK:

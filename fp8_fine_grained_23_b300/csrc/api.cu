@@ -350,6 +350,43 @@ int fp8_blockscaled_grouped_gemm_swiglu_quant(const uint8_t* a_q, const float* a
                                      G, R, N2, K, h_q, ldh, false, h_s, stream);
 }
 
+int fp8_moe_permute(const uint8_t* q, int64_t ldq, const float* s, int64_t T,
+                    const int32_t* token_of_row, int64_t R, int64_t K, uint8_t* qp, int64_t ldqp,
+                    float* sp, fp8bs_stream_t stream)
+{
+    if (T < 0 || R < 0 || K <= 0 || K % 128 != 0 || ldq < K || ldqp < K) return FP8BS_ERR_INVALID_ARG;
+    if (T > INT32_MAX || R > INT32_MAX || K > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
+    if (R == 0) return FP8BS_OK;
+    if (T == 0 || !q || !s || !token_of_row || !qp || !sp) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(qp) || ldq % 16 != 0 || ldqp % 16 != 0 || !aligned4(s) ||
+        !aligned4(sp) || !aligned4(token_of_row))
+        return FP8BS_ERR_MISALIGNED;
+    DeviceInfo* d = nullptr;
+    int st = current_device(&d);
+    if (st != FP8BS_OK) return st;
+    return cuda_status(launch_moe_permute(q, ldq, s, T, token_of_row, R, K, qp, ldqp, sp,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int fp8_moe_combine(const void* y, int64_t ldy, int64_t R, const int32_t* row_of_token,
+                    const float* weights, int64_t T, int64_t topk, int64_t N, void* out,
+                    int64_t ldo, fp8bs_stream_t stream)
+{
+    if (R < 0 || T < 0 || topk < 1 || topk > 32 || N <= 0 || N % 8 != 0 || ldy < N || ldo < N)
+        return FP8BS_ERR_INVALID_ARG;
+    if (R > INT32_MAX || T > INT32_MAX || N > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
+    if (T == 0) return FP8BS_OK;
+    if (!y || !row_of_token || !weights || !out) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned16(y) || !aligned16(out) || ldy % 8 != 0 || ldo % 8 != 0 ||
+        !aligned4(row_of_token) || !aligned4(weights))
+        return FP8BS_ERR_MISALIGNED;
+    DeviceInfo* d = nullptr;
+    int st = current_device(&d);
+    if (st != FP8BS_OK) return st;
+    return cuda_status(launch_moe_combine(y, ldy, R, row_of_token, weights, T, topk, N, out, ldo,
+                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
 int fp8bs_debug_skip_release(int at)
 {
     if (at < 0) return FP8BS_ERR_INVALID_ARG;

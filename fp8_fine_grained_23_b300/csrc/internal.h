@@ -56,6 +56,12 @@ cudaError_t launch_quant_act(const void* x, int64_t M, int64_t K, int64_t ldx, u
                              cudaStream_t stream);
 cudaError_t launch_quant_weight(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
                                 int64_t ldq, float* scales, cudaStream_t stream);
+cudaError_t launch_moe_permute(const uint8_t* q, int64_t ldq, const float* s, int64_t T,
+                               const int32_t* tok, int64_t R, int64_t K, uint8_t* qp,
+                               int64_t ldqp, float* sp, cudaStream_t stream);
+cudaError_t launch_moe_combine(const void* y, int64_t ldy, int64_t R, const int32_t* row,
+                               const float* w, int64_t T, int64_t topk, int64_t N, void* out,
+                               int64_t ldo, cudaStream_t stream);
 cudaError_t launch_quant_act_128x1(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* qt,
                                    int64_t ldqt, float* scales, cudaStream_t stream);
 cudaError_t launch_quant_weight_t(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* qt,

@@ -34,6 +34,8 @@ lib.fp8_quant_weight_128x128_t.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p, _
 lib.fp8_blockscaled_gemm_1d1d.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, _p, _i64, _int, _p]
 lib.fp8_blockscaled_grouped_gemm_swiglu_quant.argtypes = [_p, _p, _p, _p, _p, _i64, _i64, _i64,
                                                          _i64, _p, _i64, _p, _p]
+lib.fp8_moe_permute.argtypes = [_p, _i64, _p, _i64, _p, _i64, _i64, _p, _i64, _p, _p]
+lib.fp8_moe_combine.argtypes = [_p, _i64, _i64, _p, _p, _i64, _i64, _i64, _p, _i64, _p]
 lib.fp8bs_status_string.argtypes = [_int]
 lib.fp8bs_status_string.restype = ctypes.c_char_p
 lib.fp8bs_last_error.argtypes = [_p]
@@ -42,7 +44,8 @@ for _f in (lib.fp8_quant_act_1x128, lib.fp8_quant_weight_128x128, lib.fp8_blocks
            lib.fp8_blockscaled_gemm_noalloc, lib.fp8_blockscaled_grouped_gemm,
            lib.fp8bs_last_error, lib.fp8bs_debug_skip_release, lib.fp8_quant_act_128x1,
            lib.fp8_quant_weight_128x128_t, lib.fp8_blockscaled_gemm_1d1d,
-           lib.fp8_blockscaled_grouped_gemm_swiglu_quant):
+           lib.fp8_blockscaled_grouped_gemm_swiglu_quant, lib.fp8_moe_permute,
+           lib.fp8_moe_combine):
     _f.restype = _int
 
 FP8BS_OK = 0
@@ -256,6 +259,45 @@ def fp8_blockscaled_grouped_gemm_swiglu_quant(a_q: torch.Tensor, a_s: torch.Tens
                group_offsets.data_ptr(), G, R, N2, K, h_q.data_ptr(), ldh, h_s.data_ptr(),
                _stream(stream)))
     return h_q, h_s
+
+
+def fp8_moe_permute(q: torch.Tensor, s: torch.Tensor, token_of_row: torch.Tensor,
+                    qp: torch.Tensor | None = None, sp: torch.Tensor | None = None, stream=None):
+    """Gather token rows (codes q [T][K], scales s [K/128][T]) into sorted order:
+    qp [R][K] = q[token_of_row], sp [K/128][R]."""
+    T, ldq = _rows_ld(q, "q")
+    K = q.shape[1]
+    if token_of_row.dtype != torch.int32:
+        raise TypeError("token_of_row must be int32")
+    R = token_of_row.numel()
+    if qp is None:
+        qp = torch.empty(R, K, dtype=torch.uint8, device=q.device)
+    if sp is None:
+        sp = torch.empty(K // 128, R, dtype=torch.float32, device=q.device)
+    _, ldqp = _rows_ld(qp, "qp")
+    _check("fp8_moe_permute",
+           lib.fp8_moe_permute(q.data_ptr(), ldq, s.data_ptr(), T, token_of_row.data_ptr(), R, K,
+                               qp.data_ptr(), ldqp, sp.data_ptr(), _stream(stream)))
+    return qp, sp
+
+
+def fp8_moe_combine(y: torch.Tensor, row_of_token: torch.Tensor, weights: torch.Tensor,
+                    out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """out[t] = sum_j weights[t][j] * y[row_of_token[t][j]] (FP32, BF16 out); y BF16 [R][N]."""
+    if y.dtype != torch.bfloat16:
+        raise TypeError("y must be bfloat16")
+    R, ldy = _rows_ld(y, "y")
+    N = y.shape[1]
+    if row_of_token.dtype != torch.int32 or weights.dtype != torch.float32:
+        raise TypeError("row_of_token must be int32 and weights float32")
+    T, topk = row_of_token.shape
+    if out is None:
+        out = torch.empty(T, N, dtype=torch.bfloat16, device=y.device)
+    _, ldo = _rows_ld(out, "out")
+    _check("fp8_moe_combine",
+           lib.fp8_moe_combine(y.data_ptr(), ldy, R, row_of_token.data_ptr(), weights.data_ptr(),
+                               T, topk, N, out.data_ptr(), ldo, _stream(stream)))
+    return out
 
 
 def fp8bs_last_error(stream=None) -> int:

@@ -157,6 +157,39 @@ int fp8_blockscaled_grouped_gemm_swiglu_quant(const uint8_t *a_q, const float *a
                                               float *h_s, fp8bs_stream_t stream);
 
 /*
+ * MoE dispatch on the token side ([MoE]: each token is routed to 8 of 256 experts; the grouped
+ * GEMMs read rows sorted by expert). The all-to-all between GPUs is not part of this library.
+ *
+ * fp8_moe_permute: gather token rows of quantized activations into the sorted row order.
+ *   q             E4M3 codes [T][ldq] (K columns), s FP32 [K/128][T] (fp8_quant_act_1x128)
+ *   token_of_row  DEVICE int32 [R]: sorted row r holds token token_of_row[r]
+ *   qp            E4M3 codes [R][ldqp]: qp[r] = q[token_of_row[r]]
+ *   sp            FP32 [K/128][R]: sp[kb][r] = s[kb][token_of_row[r]]
+ * Bit copies. A token index outside [0, T) is outside the contract (that row is not written;
+ * nothing faults). Requires T, R >= 0 (R == 0 is a no-op), K > 0, K % 128 == 0,
+ * ldq, ldqp >= K and multiples of 16, q and qp 16-byte aligned, s, sp, token_of_row 4-byte.
+ */
+int fp8_moe_permute(const uint8_t *q, int64_t ldq, const float *s, int64_t T,
+                    const int32_t *token_of_row, int64_t R, int64_t K, uint8_t *qp, int64_t ldqp,
+                    float *sp, fp8bs_stream_t stream);
+
+/*
+ * fp8_moe_combine: each token's output is the routing-weighted sum of its expert rows,
+ *   out[t][n] = sum_j weights[t][j] * y[row_of_token[t][j]][n],
+ * accumulated in FP32 as acc = fma(weights[t][j], y, acc) for j = 0 .. topk-1 in order from 0,
+ * then rounded to BF16 (nearest, ties to even).
+ *   y             BF16 [R][ldy] (N columns): the expert outputs in sorted row order
+ *   row_of_token  DEVICE int32 [T][topk]; weights DEVICE FP32 [T][topk]
+ *   out           BF16 [T][ldo]
+ * A row index outside [0, R) adds nothing (outside the contract). Requires T >= 0 (T == 0 is a
+ * no-op), 1 <= topk <= 32, N > 0, N % 8 == 0, ldy, ldo >= N and multiples of 8, y and out
+ * 16-byte aligned, row_of_token and weights 4-byte aligned.
+ */
+int fp8_moe_combine(const void *y, int64_t ldy, int64_t R, const int32_t *row_of_token,
+                    const float *weights, int64_t T, int64_t topk, int64_t N, void *out,
+                    int64_t ldo, fp8bs_stream_t stream);
+
+/*
  * Backward pass. The pages use the same E4M3 format in the backward pass as in the forward
  * pass ([codingmall] "Định dạng E4M3 hợp nhất"; [dtcms] 三.2) and name no backward tile shapes.
  * Reading: a block-scaled contraction needs one scale per 128-long block of the contracted

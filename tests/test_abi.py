@@ -29,7 +29,7 @@ def test_header_declares_the_hot_path_calls():
     for n in ("fp8_quant_act_1x128", "fp8_quant_weight_128x128", "fp8_blockscaled_gemm",
               "fp8_blockscaled_grouped_gemm", "fp8bs_status_string", "fp8bs_last_error",
               "fp8_quant_act_128x1", "fp8_quant_weight_128x128_t", "fp8_blockscaled_gemm_1d1d",
-              "fp8_blockscaled_grouped_gemm_swiglu_quant"):
+              "fp8_blockscaled_grouped_gemm_swiglu_quant", "fp8_moe_permute", "fp8_moe_combine"):
         assert n in names
 
 
@@ -133,6 +133,22 @@ def test_swiglu_quant_argument_checks(F):
     assert f(*ok[:9], P16 + 4, *ok[10:], None) == -2                              # h_q alignment
     assert f(*ok[:11], P4 + 1, None) == -2                                        # h_s alignment
     assert f(*ok[:11], None, None) == -1                                          # no h_s
+
+
+def test_moe_dispatch_argument_checks(F):
+    pm = F.lib.fp8_moe_permute
+    assert pm(P16, 256, P4, 8, P4, 0, 256, P16, 256, P4, None) == 0               # R == 0
+    assert pm(P16, 256, P4, 8, P4, 4, 200, P16, 256, P4, None) == -1              # K % 128
+    assert pm(P16, 128, P4, 8, P4, 4, 256, P16, 256, P4, None) == -1              # ldq < K
+    assert pm(P16, 264, P4, 8, P4, 4, 256, P16, 256, P4, None) == -2              # ldq % 16
+    assert pm(P16 + 8, 256, P4, 8, P4, 4, 256, P16, 256, P4, None) == -2          # q alignment
+    cm = F.lib.fp8_moe_combine
+    assert cm(P16, 64, 8, P4, P4, 0, 8, 64, P16, 64, None) == 0                   # T == 0
+    assert cm(P16, 64, 8, P4, P4, 4, 0, 64, P16, 64, None) == -1                  # topk < 1
+    assert cm(P16, 64, 8, P4, P4, 4, 33, 64, P16, 64, None) == -1                 # topk > 32
+    assert cm(P16, 64, 8, P4, P4, 4, 8, 60, P16, 64, None) == -1                  # N % 8
+    assert cm(P16, 68, 8, P4, P4, 4, 8, 64, P16, 64, None) == -2                  # ldy % 8
+    assert cm(P16 + 4, 64, 8, P4, P4, 4, 8, 64, P16, 64, None) == -2              # y alignment
 
 
 def test_debug_hook_rejects_negative_index(F):
