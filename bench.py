@@ -424,6 +424,21 @@ def run_extras(F, dev, peaks, fp8_peak):
                            "frac_fp8_peak": round(tf / fp8_peak, 4), "N_run": w.shape[0]}
         del a, w, aq, a_s, wq, w_s, c
     out["mla_gemm"] = mla
+    # decode-size GEMMs (few rows of A): bound by streaming the weights once
+    dec = {}
+    for (N, K, seed) in ((WL.DENSE.N, WL.DENSE.K, WL.DENSE.seed), (1536, 7168, 2), (24576, 1536, 4)):
+        g = WL.generator(seed, dev)
+        wq, w_s = F.fp8_quant_weight_128x128(WL.weights(N, K, g, dev))
+        for M in (1, 16, 64):
+            aq, a_s = F.fp8_quant_act_1x128(WL.activations(M, K, g, dev))
+            c = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+            ms = _timed(lambda: F.fp8_blockscaled_gemm(aq, a_s, wq, w_s, out=c), dev)
+            byts = wq.numel() + w_s.numel() * 4 + aq.numel() + a_s.numel() * 4 + c.numel() * 2
+            gbs = byts / (ms * 1e-3) / 1e9
+            dec[f"{M}x{N}x{K}"] = {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
+                                   "frac_hbm": round(gbs / hbm, 4)}
+        del wq, w_s, aq, a_s, c
+    out["decode_gemm"] = dec
     # MoE grouped GEMMs: gate+up and down alone (BF16 out), the gate+up GEMM with the fused
     # SwiGLU + 1x128 re-quantization, and the expert FFN chain (fused gate+up, then down on h)
     moe = {}

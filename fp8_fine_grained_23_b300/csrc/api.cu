@@ -168,6 +168,34 @@ int dense_gemm(GemmKind kind, const uint8_t* a_q, const float* a_s, const uint8_
     if ((st = ensure_error_word(d)) != FP8BS_OK) return st;
     if ((st = ensure_encoder()) != FP8BS_OK) return st;
 
+    if (kind == GemmKind::DENSE && M <= GEMM_SMALL_MAX_M) {
+        // Few rows: the weight rows take the tensor core's 128-row side, the M rows its narrow
+        // side; the K loop is split over a cluster while the weight tiles cannot cover the SMs.
+        const int bnt = gemm_small_tokens(M);
+        CUtensorMap mw, ma;
+        if ((st = make_code_map(&mw, w_q, K, N, K, 128)) != FP8BS_OK) return st;
+        if ((st = make_code_map(&ma, a_q, K, M, K, bnt)) != FP8BS_OK) return st;
+        SmallArgs sa{};
+        sa.a_s = a_s;
+        sa.w_s = w_s;
+        sa.c = c;
+        sa.ldc = ldc;
+        sa.M = static_cast<int>(M);
+        sa.N = static_cast<int>(N);
+        sa.KB = static_cast<int>(K / 128);
+        sa.n_tiles = static_cast<int>((N + 127) / 128);
+        sa.m_tiles = static_cast<int>((M + bnt - 1) / bnt);
+        sa.split = 1;
+        const int64_t items = static_cast<int64_t>(sa.n_tiles) * sa.m_tiles;
+        while (sa.split < 8 && items * sa.split * 2 <= d->num_sms && sa.KB >= 4 * sa.split)
+            sa.split *= 2;
+        if (items * sa.split > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
+        sa.err = d->err;
+        sa.budget = wait_budget();
+        return cuda_status(launch_gemm_small(mw, ma, sa, bnt, out_dtype == FP8BS_OUT_F32,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+    }
+
     const int cluster = gemm_cluster_size(false);
     CUtensorMap ma, mb;
     if ((st = make_code_map(&ma, a_q, K, M, K, GEMM_BM)) != FP8BS_OK) return st;

@@ -71,6 +71,26 @@ cudaError_t launch_quant_weight_t(const void* w, int64_t N, int64_t K, int64_t l
 // GEMM launch, then back to -1.
 int take_fault_skip_release();
 
+// Few-row GEMM (M <= GEMM_SMALL_MAX_M) computed as C^T = W A^T with split-K over a cluster (gemm_small.cu).
+struct SmallArgs {
+    const float* a_s;         // [K/128][M]
+    const float* w_s;         // [ceil(N/128)][K/128]
+    void* c;                  // [M][ldc]
+    int64_t ldc;
+    int M;
+    int N;
+    int KB;                   // K / 128
+    int n_tiles;              // ceil(N / 128): weight-row tiles
+    int m_tiles;              // ceil(M / tokens per tile)
+    int split;                // CTAs per cluster sharing one tile's K loop (1, 2, 4 or 8)
+    int* err;
+    long long budget;
+};
+constexpr int GEMM_SMALL_MAX_M = 64;   // above this the tiled CTA-pair kernel is faster
+int gemm_small_tokens(int64_t M);   // tokens per tile for M rows: 32 or 64 (128 kept for tests)
+cudaError_t launch_gemm_small(const CUtensorMap& map_w, const CUtensorMap& map_a,
+                              const SmallArgs& args, int bnt, bool out_f32, cudaStream_t stream);
+
 // DENSE: per-128x128-block B scales; GROUPED: the same per expert; ROW_SCALED: a scale per B
 // row and K block (the 1d1d weight-gradient GEMM), dense only.
 // GROUPED_SWIGLU: grouped, gate/up rows interleaved per 128, epilogue silu(gate) * up re-quantized

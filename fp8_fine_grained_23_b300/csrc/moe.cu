@@ -64,7 +64,7 @@ moe_permute_kernel(const uint8_t* __restrict__ q, int64_t ldq, const float* __re
 }
 
 // Token t = one warp: out[t][n] = sum_j w[t][j] * y[row[t][j]][n] as an FP32 fma chain in
-// j order from 0, rounded to BF16 (nearest even). Lane l handles columns 8 (l + 32 i) .. + 7.
+// j order from 0, rounded to BF16 (nearest even).
 // A row index outside [0, R) adds nothing (outside the contract).
 __global__ void __launch_bounds__(MOE_THREADS)
 moe_combine_kernel(const uint16_t* __restrict__ y, int64_t ldy, int64_t R,
@@ -82,30 +82,63 @@ moe_combine_kernel(const uint16_t* __restrict__ y, int64_t ldy, int64_t R,
         my_row = (rv >= 0 && rv < R) ? rv : -1;
         my_w = w[t * topk + lane];
     }
-    for (int c = lane; c < N / 8; c += 32) {
-        float acc[8];
+    // A warp step covers 2 KB of every row it reads (lane l: 16-byte chunks 4 l .. 4 l + 3 of
+    // the step), so the gathered rows reach DRAM in long runs; rows go 4 at a time, their loads
+    // issued before their fma chains.
+    const int chunks = N / 8;
+    for (int c0 = 0; c0 < chunks; c0 += 128) {
+        float acc[4][8];
 #pragma unroll
-        for (int e = 0; e < 8; e++) acc[e] = 0.0f;
-        for (int j = 0; j < topk; j++) {
-            const int64_t rj = __shfl_sync(0xffffffffu, my_row, j);
-            const float wj = __shfl_sync(0xffffffffu, my_w, j);
-            if (rj < 0) continue;
-            const uint4 v = ld_nc_v4(y + rj * ldy + 8 * c);
-            const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+        for (int q = 0; q < 4; q++)
 #pragma unroll
-            for (int e = 0; e < 4; e++) {
-                acc[2 * e] = __fmaf_rn(wj, __uint_as_float(wd[e] << 16), acc[2 * e]);
-                acc[2 * e + 1] = __fmaf_rn(wj, __uint_as_float(wd[e] & 0xFFFF0000u), acc[2 * e + 1]);
+            for (int e = 0; e < 8; e++) acc[q][e] = 0.0f;
+        for (int j0 = 0; j0 < topk; j0 += 4) {
+            uint4 v[4][4];
+            float wj[4];
+#pragma unroll
+            for (int jj = 0; jj < 4; jj++) {
+                const int j = j0 + jj;
+                const int64_t rj = __shfl_sync(0xffffffffu, my_row, j & 31);
+                const bool use = j < topk && rj >= 0;
+                wj[jj] = use ? __shfl_sync(0xffffffffu, my_w, j & 31) : 0.0f;
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    const int c = c0 + 4 * lane + q;
+                    v[jj][q] = (use && c < chunks) ? ld_nc_v4(y + rj * ldy + 8 * c)
+                                                   : make_uint4(0, 0, 0, 0);
+                }
+            }
+#pragma unroll
+            for (int jj = 0; jj < 4; jj++) {
+                if (j0 + jj >= topk) break;
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    const uint32_t wd[4] = {v[jj][q].x, v[jj][q].y, v[jj][q].z, v[jj][q].w};
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        acc[q][2 * e] =
+                            __fmaf_rn(wj[jj], __uint_as_float(wd[e] << 16), acc[q][2 * e]);
+                        acc[q][2 * e + 1] = __fmaf_rn(wj[jj], __uint_as_float(wd[e] & 0xFFFF0000u),
+                                                      acc[q][2 * e + 1]);
+                    }
+                }
             }
         }
-        uint32_t o[4];
 #pragma unroll
-        for (int e = 0; e < 4; e++) {
-            uint32_t packed;
-            asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(packed) : "f"(acc[2 * e + 1]), "f"(acc[2 * e]));
-            o[e] = packed;
+        for (int q = 0; q < 4; q++) {
+            const int c = c0 + 4 * lane + q;
+            if (c >= chunks) continue;
+            uint32_t o[4];
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                uint32_t packed;
+                asm("cvt.rn.bf16x2.f32 %0, %1, %2;"
+                    : "=r"(packed)
+                    : "f"(acc[q][2 * e + 1]), "f"(acc[q][2 * e]));
+                o[e] = packed;
+            }
+            st_v4_global(out + t * ldo + 8 * c, make_uint4(o[0], o[1], o[2], o[3]));
         }
-        st_v4_global(out + t * ldo + 8 * c, make_uint4(o[0], o[1], o[2], o[3]));
     }
 }
 
