@@ -162,6 +162,37 @@ static tile_scale_t tile_scale(float amax)
     return t;
 }
 
+/* Power-of-two (UE8M0) tile scale, a variant that is not on the pages (Blackwell's block-scaled
+ * MMAs take such scales): s = 2^e with e the smallest integer for which 448 * 2^e >= amax, so that
+ * no value saturates, clamped below at UE8M0's 2^-127; codes E4M3(x * 2^-e), an exact scaling.
+ * With amax = f * 2^E (frexp, f in [0.5, 1)) and 448 = 0.875 * 2^9, e = E - 9 + (f > 0.875). */
+static int ue8m0_exponent(float amax)
+{
+    int E;
+    float f = frexpf(amax, &E);
+    int e = E - 9 + (f > 0.875f ? 1 : 0);
+    return e < -127 ? -127 : e;
+}
+
+static tile_scale_t tile_scale_ue8m0(float amax)
+{
+    tile_scale_t t;
+    t.tiny = 0;
+    t.zero = 0;
+    if (amax == 0.0f) {
+        t.s = 1.0f;
+        t.r = 0.0f;
+        t.zero = 1;
+        return t;
+    }
+    int e = ue8m0_exponent(amax);
+    t.s = ldexpf(1.0f, e);
+    t.r = ldexpf(1.0f, -e);
+    return t;
+}
+
+int orc_ue8m0_exponent(float amax) { return ue8m0_exponent(amax); }
+
 static uint8_t tile_encode(float x, const tile_scale_t *t)
 {
     float y;
@@ -173,8 +204,8 @@ static uint8_t tile_encode(float x, const tile_scale_t *t)
 
 /* 1x128 activation tiles: one scale per row m and 128-column block kb.
  * x: BF16 bits [M][ldx]; q: codes [M][ldq]; s: [K/128][M]. K must be a multiple of 128. */
-void orc_quant_act_1x128(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
-                         uint8_t *q, int64_t ldq, float *s)
+static void quant_act_1x128(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                            uint8_t *q, int64_t ldq, float *s, int ue8m0)
 {
     int64_t KB = K / 128;
     for (int64_t m = 0; m < M; m++) {
@@ -185,7 +216,7 @@ void orc_quant_act_1x128(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
             tile_scale_t t;
             for (int k = 0; k < 128; k++)
                 amax = fmaxf(amax, fabsf(bf16_bits_to_float(xt[k])));
-            t = tile_scale(amax);
+            t = ue8m0 ? tile_scale_ue8m0(amax) : tile_scale(amax);
             for (int k = 0; k < 128; k++)
                 qt[k] = tile_encode(bf16_bits_to_float(xt[k]), &t);
             s[kb * M + m] = t.s;
@@ -193,11 +224,24 @@ void orc_quant_act_1x128(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
     }
 }
 
+void orc_quant_act_1x128(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                         uint8_t *q, int64_t ldq, float *s)
+{
+    quant_act_1x128(x, M, K, ldx, q, ldq, s, 0);
+}
+
+/* The same tiles with power-of-two scales (tile_scale_ue8m0). */
+void orc_quant_act_1x128_ue8m0(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                               uint8_t *q, int64_t ldq, float *s)
+{
+    quant_act_1x128(x, M, K, ldx, q, ldq, s, 1);
+}
+
 /* 128x128 weight blocks: one scale per (128 rows of N) x (128 columns of K).
  * w: BF16 bits [N][ldw]; q: codes [N][ldq]; s: [ceil(N/128)][K/128].
  * The last row block may be partial; its amax covers only rows < N. */
-void orc_quant_weight_128x128(const uint16_t *w, int64_t N, int64_t K, int64_t ldw,
-                              uint8_t *q, int64_t ldq, float *s)
+static void quant_weight_128x128(const uint16_t *w, int64_t N, int64_t K, int64_t ldw,
+                                 uint8_t *q, int64_t ldq, float *s, int ue8m0)
 {
     int64_t KB = K / 128;
     int64_t NB = (N + 127) / 128;
@@ -209,7 +253,7 @@ void orc_quant_weight_128x128(const uint16_t *w, int64_t N, int64_t K, int64_t l
             for (int64_t n = nb * 128; n < n_end; n++)
                 for (int k = 0; k < 128; k++)
                     amax = fmaxf(amax, fabsf(bf16_bits_to_float(w[n * ldw + kb * 128 + k])));
-            t = tile_scale(amax);
+            t = ue8m0 ? tile_scale_ue8m0(amax) : tile_scale(amax);
             for (int64_t n = nb * 128; n < n_end; n++)
                 for (int k = 0; k < 128; k++)
                     q[n * ldq + kb * 128 + k] =
@@ -217,6 +261,19 @@ void orc_quant_weight_128x128(const uint16_t *w, int64_t N, int64_t K, int64_t l
             s[nb * KB + kb] = t.s;
         }
     }
+}
+
+void orc_quant_weight_128x128(const uint16_t *w, int64_t N, int64_t K, int64_t ldw,
+                              uint8_t *q, int64_t ldq, float *s)
+{
+    quant_weight_128x128(w, N, K, ldw, q, ldq, s, 0);
+}
+
+/* The same blocks with power-of-two scales (tile_scale_ue8m0). */
+void orc_quant_weight_128x128_ue8m0(const uint16_t *w, int64_t N, int64_t K, int64_t ldw,
+                                    uint8_t *q, int64_t ldq, float *s)
+{
+    quant_weight_128x128(w, N, K, ldw, q, ldq, s, 1);
 }
 
 /* 128x1 activation tiles for the weight-gradient GEMM: one scale per 128 consecutive rows

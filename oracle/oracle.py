@@ -68,6 +68,10 @@ def lib() -> ctypes.CDLL:
             L.orc_gemm_1d1d_points.argtypes = [_p, _i64, _p, _p, _i64, _p, _i64, _i64, _i64,
                                                _i64, _p, _p, _p, _p, _p]
             L.orc_swiglu_f64.argtypes = [_p, _p, _i64, _p]
+            L.orc_quant_act_1x128_ue8m0.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p]
+            L.orc_quant_weight_128x128_ue8m0.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p]
+            L.orc_ue8m0_exponent.argtypes = [ctypes.c_float]
+            L.orc_ue8m0_exponent.restype = ctypes.c_int
             L.orc_moe_permute.argtypes = [_p, _i64, _p, _i64, _p, _i64, _i64, _p, _i64, _p]
             L.orc_moe_combine.argtypes = [_p, _i64, _p, _p, _i64, _i64, _i64, _p, _i64]
             for f in (L.orc_e4m3_encode_array, L.orc_e4m3_decode_array, L.orc_quant_act_1x128,
@@ -75,7 +79,8 @@ def lib() -> ctypes.CDLL:
                       L.orc_grouped_gemm_points, L.orc_gemm_unquantized_f64,
                       L.orc_quant_act_128x1, L.orc_quant_weight_128x128_t,
                       L.orc_gemm_1d1d_points, L.orc_swiglu_f64, L.orc_moe_permute,
-                      L.orc_moe_combine):
+                      L.orc_moe_combine, L.orc_quant_act_1x128_ue8m0,
+                      L.orc_quant_weight_128x128_ue8m0):
                 f.restype = None
             _lib = L
         return _lib
@@ -133,6 +138,33 @@ def quant_weight_128x128(w_bits) -> tuple[np.ndarray, np.ndarray]:
     q = np.empty((N, K), np.uint8)
     s = np.empty(((N + 127) // 128, K // 128), np.float32)
     lib().orc_quant_weight_128x128(_ptr(w), N, K, K, _ptr(q), K, _ptr(s))
+    return q, s
+
+
+def ue8m0_exponent(amax: float) -> int:
+    """e of the power-of-two tile scale 2^e for a tile maximum amax > 0 (see fp8_oracle.c)."""
+    return int(lib().orc_ue8m0_exponent(ctypes.c_float(amax)))
+
+
+def quant_act_1x128_ue8m0(x_bits) -> tuple[np.ndarray, np.ndarray]:
+    """quant_act_1x128 with power-of-two (UE8M0) tile scales; same layouts."""
+    x = _c(x_bits, np.uint16)
+    M, K = x.shape
+    assert K % 128 == 0
+    q = np.empty((M, K), np.uint8)
+    s = np.empty((K // 128, M), np.float32)
+    lib().orc_quant_act_1x128_ue8m0(_ptr(x), M, K, K, _ptr(q), K, _ptr(s))
+    return q, s
+
+
+def quant_weight_128x128_ue8m0(w_bits) -> tuple[np.ndarray, np.ndarray]:
+    """quant_weight_128x128 with power-of-two (UE8M0) block scales; same layouts."""
+    w = _c(w_bits, np.uint16)
+    N, K = w.shape
+    assert K % 128 == 0
+    q = np.empty((N, K), np.uint8)
+    s = np.empty(((N + 127) // 128, K // 128), np.float32)
+    lib().orc_quant_weight_128x128_ue8m0(_ptr(w), N, K, K, _ptr(q), K, _ptr(s))
     return q, s
 
 
