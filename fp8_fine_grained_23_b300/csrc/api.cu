@@ -271,6 +271,32 @@ int grouped_gemm(GemmKind kind, const uint8_t* a_q, const float* a_s, const uint
         launch_gemm(ma, mb, args, kind, out_f32, max_ctas, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// The two tile quantizers, with amax/448 or power-of-two (ue8m0) scales.
+int quant_act(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, int64_t ldq,
+              float* scales, bool ue8m0, fp8bs_stream_t stream)
+{
+    int st = check_quant_args(x, M, K, ldx, q, ldq, scales);
+    if (st != FP8BS_OK || M == 0) return st;
+    DeviceInfo* d = nullptr;
+    if ((st = current_device(&d)) != FP8BS_OK) return st;
+    if ((st = ensure_error_word(d)) != FP8BS_OK) return st;
+    return cuda_status(launch_quant_act(x, M, K, ldx, q, ldq, scales, d->num_sms, d->err,
+                                        wait_budget(), ue8m0,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int quant_weight(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q, int64_t ldq,
+                 float* scales, bool ue8m0, fp8bs_stream_t stream)
+{
+    int st = check_quant_args(w, N, K, ldw, q, ldq, scales);
+    if (st != FP8BS_OK || N == 0) return st;
+    if ((N + 127) / 128 > 65535) return FP8BS_ERR_INVALID_ARG;   // grid.y limit
+    DeviceInfo* d = nullptr;
+    if ((st = current_device(&d)) != FP8BS_OK) return st;
+    return cuda_status(launch_quant_weight(w, N, K, ldw, q, ldq, scales, ue8m0,
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace host
 
 int take_fault_skip_release()
@@ -288,25 +314,25 @@ extern "C" {
 int fp8_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, int64_t ldq,
                         float* scales, fp8bs_stream_t stream)
 {
-    int st = check_quant_args(x, M, K, ldx, q, ldq, scales);
-    if (st != FP8BS_OK || M == 0) return st;
-    DeviceInfo* d = nullptr;
-    if ((st = current_device(&d)) != FP8BS_OK) return st;
-    if ((st = ensure_error_word(d)) != FP8BS_OK) return st;
-    return cuda_status(launch_quant_act(x, M, K, ldx, q, ldq, scales, d->num_sms, d->err,
-                                        wait_budget(), reinterpret_cast<cudaStream_t>(stream)));
+    return fp8bs::host::quant_act(x, M, K, ldx, q, ldq, scales, false, stream);
+}
+
+int fp8_quant_act_1x128_ue8m0(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
+                              int64_t ldq, float* scales, fp8bs_stream_t stream)
+{
+    return fp8bs::host::quant_act(x, M, K, ldx, q, ldq, scales, true, stream);
 }
 
 int fp8_quant_weight_128x128(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
                              int64_t ldq, float* scales, fp8bs_stream_t stream)
 {
-    int st = check_quant_args(w, N, K, ldw, q, ldq, scales);
-    if (st != FP8BS_OK || N == 0) return st;
-    if ((N + 127) / 128 > 65535) return FP8BS_ERR_INVALID_ARG;   // grid.y limit
-    DeviceInfo* d = nullptr;
-    if ((st = current_device(&d)) != FP8BS_OK) return st;
-    return cuda_status(
-        launch_quant_weight(w, N, K, ldw, q, ldq, scales, reinterpret_cast<cudaStream_t>(stream)));
+    return fp8bs::host::quant_weight(w, N, K, ldw, q, ldq, scales, false, stream);
+}
+
+int fp8_quant_weight_128x128_ue8m0(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
+                                   int64_t ldq, float* scales, fp8bs_stream_t stream)
+{
+    return fp8bs::host::quant_weight(w, N, K, ldw, q, ldq, scales, true, stream);
 }
 
 int fp8_blockscaled_gemm(const uint8_t* a_q, const float* a_s, const uint8_t* w_q,

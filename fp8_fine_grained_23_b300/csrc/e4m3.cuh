@@ -29,6 +29,30 @@ __device__ __forceinline__ TileScale tile_scale(float amax)
     return t;
 }
 
+// Power-of-two (UE8M0) tile scale, a variant that is not on the pages (Blackwell's block-scaled
+// MMAs take such scales): s = 2^e with e the smallest integer for which 448 * 2^e >= amax (no value
+// saturates), clamped below at 2^-127; r = 2^-e, so x * r is exact. With amax = f * 2^E (frexpf,
+// f in [0.5, 1)) and 448 = 0.875 * 2^9: e = E - 9 + (f > 0.875).
+__device__ __forceinline__ TileScale tile_scale_ue8m0(float amax)
+{
+    TileScale t;
+    t.zero = (amax == 0.0f);
+    t.tiny = false;
+    int E;
+    const float f = frexpf(amax, &E);
+    int e = E - 9 + (f > 0.875f ? 1 : 0);
+    e = e < -127 ? -127 : e;
+    t.s = t.zero ? 1.0f : ldexpf(1.0f, e);
+    t.r = t.zero ? 0.0f : ldexpf(1.0f, -e);
+    return t;
+}
+
+template <bool UE8M0>
+__device__ __forceinline__ TileScale tile_scale_of(float amax)
+{
+    return UE8M0 ? tile_scale_ue8m0(amax) : tile_scale(amax);
+}
+
 // Two FP32 values to two E4M3 codes, saturating round-to-nearest-even; `lo` lands in the low
 // byte of the result.
 __device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi)

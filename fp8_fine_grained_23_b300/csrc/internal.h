@@ -51,11 +51,12 @@ struct GemmArgs {
                               // its TMEM release (-1: never); set by fp8bs_debug_skip_release
 };
 
+// ue8m0: power-of-two tile scales (tile_scale_ue8m0) instead of amax / 448
 cudaError_t launch_quant_act(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
                              int64_t ldq, float* scales, int num_sms, int* err, long long budget,
-                             cudaStream_t stream);
+                             bool ue8m0, cudaStream_t stream);
 cudaError_t launch_quant_weight(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
-                                int64_t ldq, float* scales, cudaStream_t stream);
+                                int64_t ldq, float* scales, bool ue8m0, cudaStream_t stream);
 cudaError_t launch_moe_permute(const uint8_t* q, int64_t ldq, const float* s, int64_t T,
                                const int32_t* tok, int64_t R, int64_t K, uint8_t* qp,
                                int64_t ldqp, float* sp, cudaStream_t stream);

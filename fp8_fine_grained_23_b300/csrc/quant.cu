@@ -158,6 +158,7 @@ __device__ __forceinline__ uint32_t qa_phase(int64_t i)
     return static_cast<uint32_t>((i / QA_CONSUMERS) / QA_SLOTS_PER_WARP) & 1u;
 }
 
+template <bool UE8M0>
 __global__ void __launch_bounds__(QA_THREADS, QA_CTAS_PER_SM)
 quant_act_1x128_kernel(const QuantActArgs p)
 {
@@ -247,7 +248,7 @@ quant_act_1x128_kernel(const QuantActArgs p)
 #pragma unroll
             for (int j = 0; j < 16; j++) m2 = absmax_bits_u16x2(v[j], m2);
             const uint32_t mbits = max(m2 & 0xFFFFu, m2 >> 16);
-            const TileScale ts = tile_scale(__uint_as_float(mbits << 16));
+            const TileScale ts = tile_scale_of<UE8M0>(__uint_as_float(mbits << 16));
             __syncwarp();   // every lane holds its tile before the codes overwrite the slot
 
 #pragma unroll
@@ -280,6 +281,7 @@ quant_act_1x128_kernel(const QuantActArgs p)
 // Thread t reads 16 bytes of rows (t/16) + 16 i, i = 0..7, so the block is read from HBM once
 // and held in registers while its amax is reduced (warp shuffles, then shared memory).
 // ------------------------------------------------------------------------------------
+template <bool UE8M0>
 __global__ void __launch_bounds__(QUANT_THREADS)
 quant_weight_128x128_kernel(const uint16_t* __restrict__ w, int64_t N, int KB, int64_t ldw,
                             uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ scales)
@@ -314,7 +316,7 @@ quant_weight_128x128_kernel(const uint16_t* __restrict__ w, int64_t N, int KB, i
 #pragma unroll
     for (int i = 1; i < QUANT_THREADS / 32; i++) a = fmaxf(a, red[i]);
 
-    const TileScale ts = tile_scale(a);
+    const TileScale ts = tile_scale_of<UE8M0>(a);
 #pragma unroll
     for (int i = 0; i < 8; i++) {
         const int64_t row = nb * 128 + r0 + 16 * i;
@@ -451,7 +453,7 @@ quant_transpose_kernel(const uint16_t* __restrict__ x, int64_t ldx, uint8_t* __r
 
 cudaError_t launch_quant_act(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
                              int64_t ldq, float* scales, int num_sms, int* err, long long budget,
-                             cudaStream_t stream)
+                             bool ue8m0, cudaStream_t stream)
 {
     QuantActArgs a;
     a.x = static_cast<const uint16_t*>(x);
@@ -466,21 +468,22 @@ cudaError_t launch_quant_act(const void* x, int64_t M, int64_t K, int64_t ldx, u
     const int64_t segs = M * ((a.KB + SEG_TILES - 1) / SEG_TILES);
     const int64_t cap = static_cast<int64_t>(num_sms) * QA_CTAS_PER_SM;
     const int grid = static_cast<int>(segs < cap ? segs : cap);
-    cudaError_t e = cudaFuncSetAttribute(quant_act_1x128_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, QA_SMEM);
+    auto kern = ue8m0 ? quant_act_1x128_kernel<true> : quant_act_1x128_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, QA_SMEM);
     if (e != cudaSuccess) return e;
-    quant_act_1x128_kernel<<<grid, QA_THREADS, QA_SMEM, stream>>>(a);
+    kern<<<grid, QA_THREADS, QA_SMEM, stream>>>(a);
     return cudaGetLastError();
 }
 
 cudaError_t launch_quant_weight(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
-                                int64_t ldq, float* scales, cudaStream_t stream)
+                                int64_t ldq, float* scales, bool ue8m0, cudaStream_t stream)
 {
     const int KB = static_cast<int>(K / 128);
     const int64_t NB = (N + 127) / 128;
     dim3 grid(KB, static_cast<unsigned>(NB));
-    quant_weight_128x128_kernel<<<grid, QUANT_THREADS, 0, stream>>>(
-        static_cast<const uint16_t*>(w), N, KB, ldw, q, ldq, scales);
+    auto kern = ue8m0 ? quant_weight_128x128_kernel<true> : quant_weight_128x128_kernel<false>;
+    kern<<<grid, QUANT_THREADS, 0, stream>>>(static_cast<const uint16_t*>(w), N, KB, ldw, q, ldq,
+                                             scales);
     return cudaGetLastError();
 }
 

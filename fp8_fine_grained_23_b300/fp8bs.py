@@ -24,6 +24,8 @@ lib = ctypes.CDLL(LIB_PATH)
 _i64, _p, _int = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
 lib.fp8_quant_act_1x128.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p, _p]
 lib.fp8_quant_weight_128x128.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p, _p]
+lib.fp8_quant_act_1x128_ue8m0.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p, _p]
+lib.fp8_quant_weight_128x128_ue8m0.argtypes = [_p, _i64, _i64, _i64, _p, _i64, _p, _p]
 lib.fp8_blockscaled_gemm.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, _p, _i64, _int, _p]
 lib.fp8_blockscaled_gemm_noalloc.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, _p, _i64, _int,
                                              _p]
@@ -45,7 +47,8 @@ for _f in (lib.fp8_quant_act_1x128, lib.fp8_quant_weight_128x128, lib.fp8_blocks
            lib.fp8bs_last_error, lib.fp8bs_debug_skip_release, lib.fp8_quant_act_128x1,
            lib.fp8_quant_weight_128x128_t, lib.fp8_blockscaled_gemm_1d1d,
            lib.fp8_blockscaled_grouped_gemm_swiglu_quant, lib.fp8_moe_permute,
-           lib.fp8_moe_combine):
+           lib.fp8_moe_combine, lib.fp8_quant_act_1x128_ue8m0,
+           lib.fp8_quant_weight_128x128_ue8m0):
     _f.restype = _int
 
 FP8BS_OK = 0
@@ -88,7 +91,7 @@ def _rows_ld(t: torch.Tensor, name: str) -> tuple[int, int]:
 
 
 def fp8_quant_act_1x128(x: torch.Tensor, q: torch.Tensor | None = None,
-                        scales: torch.Tensor | None = None, stream=None):
+                        scales: torch.Tensor | None = None, stream=None, _fn=None):
     """E4M3 codes [M][K] (uint8) and FP32 scales [K/128][M] of BF16 activations x [M][K]."""
     if x.dtype != torch.bfloat16:
         raise TypeError("x must be bfloat16")
@@ -99,14 +102,20 @@ def fp8_quant_act_1x128(x: torch.Tensor, q: torch.Tensor | None = None,
     if scales is None:
         scales = torch.empty(K // 128, M, dtype=torch.float32, device=x.device)
     _, ldq = _rows_ld(q, "q")
-    _check("fp8_quant_act_1x128",
-           lib.fp8_quant_act_1x128(x.data_ptr(), M, K, ldx, q.data_ptr(), ldq, scales.data_ptr(),
-                                   _stream(stream)))
+    fn = _fn or lib.fp8_quant_act_1x128
+    _check(fn.__name__, fn(x.data_ptr(), M, K, ldx, q.data_ptr(), ldq, scales.data_ptr(),
+                           _stream(stream)))
     return q, scales
 
 
+def fp8_quant_act_1x128_ue8m0(x: torch.Tensor, q: torch.Tensor | None = None,
+                              scales: torch.Tensor | None = None, stream=None):
+    """fp8_quant_act_1x128 with power-of-two (UE8M0) tile scales."""
+    return fp8_quant_act_1x128(x, q, scales, stream, _fn=lib.fp8_quant_act_1x128_ue8m0)
+
+
 def fp8_quant_weight_128x128(w: torch.Tensor, q: torch.Tensor | None = None,
-                             scales: torch.Tensor | None = None, stream=None):
+                             scales: torch.Tensor | None = None, stream=None, _fn=None):
     """E4M3 codes [N][K] and FP32 scales [ceil(N/128)][K/128] of BF16 weights w [N][K]."""
     if w.dtype != torch.bfloat16:
         raise TypeError("w must be bfloat16")
@@ -117,10 +126,16 @@ def fp8_quant_weight_128x128(w: torch.Tensor, q: torch.Tensor | None = None,
     if scales is None:
         scales = torch.empty((N + 127) // 128, K // 128, dtype=torch.float32, device=w.device)
     _, ldq = _rows_ld(q, "q")
-    _check("fp8_quant_weight_128x128",
-           lib.fp8_quant_weight_128x128(w.data_ptr(), N, K, ldw, q.data_ptr(), ldq,
-                                        scales.data_ptr(), _stream(stream)))
+    fn = _fn or lib.fp8_quant_weight_128x128
+    _check(fn.__name__, fn(w.data_ptr(), N, K, ldw, q.data_ptr(), ldq, scales.data_ptr(),
+                           _stream(stream)))
     return q, scales
+
+
+def fp8_quant_weight_128x128_ue8m0(w: torch.Tensor, q: torch.Tensor | None = None,
+                                   scales: torch.Tensor | None = None, stream=None):
+    """fp8_quant_weight_128x128 with power-of-two (UE8M0) block scales."""
+    return fp8_quant_weight_128x128(w, q, scales, stream, _fn=lib.fp8_quant_weight_128x128_ue8m0)
 
 
 def fp8_quant_act_128x1(x: torch.Tensor, qt: torch.Tensor | None = None,

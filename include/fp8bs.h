@@ -87,6 +87,20 @@ int fp8_quant_weight_128x128(const void *w, int64_t N, int64_t K, int64_t ldw,
                              uint8_t *q, int64_t ldq, float *scales, fp8bs_stream_t stream);
 
 /*
+ * fp8_quant_act_1x128_ue8m0 / fp8_quant_weight_128x128_ue8m0: the same tiles, layouts and
+ * requirements as fp8_quant_act_1x128 / fp8_quant_weight_128x128, with power-of-two scales.
+ * This variant is not on the pages (their scale is amax/448); power-of-two (UE8M0) scales are
+ * what Blackwell's block-scaled MMAs consume, and these calls let their numerics be compared:
+ *   s = 2^e, e the smallest integer with 448 * 2^e >= amax (no value saturates), clamped below
+ *   at e = -127; codes E4M3(x * 2^-e) (an exact scaling); a zero tile gets s = 1, codes 0x00.
+ * The scales are ordinary FP32 values, so every GEMM call accepts them unchanged.
+ */
+int fp8_quant_act_1x128_ue8m0(const void *x, int64_t M, int64_t K, int64_t ldx,
+                              uint8_t *q, int64_t ldq, float *scales, fp8bs_stream_t stream);
+int fp8_quant_weight_128x128_ue8m0(const void *w, int64_t N, int64_t K, int64_t ldw,
+                                   uint8_t *q, int64_t ldq, float *scales, fp8bs_stream_t stream);
+
+/*
  * Block-scaled FP8 GEMM, C = A W^T ([dtcms] 三.1: FP8 inputs, BF16 or FP32 output;
  * [codingmall] "Tăng độ chính xác tích lũy": partial sums promoted to FP32 at intervals).
  *   C[m][n] = sum_kb  a_s[kb*M + m] * w_s[(n/128)*(K/128) + kb] * P[m][n][kb],
