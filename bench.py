@@ -19,6 +19,7 @@ bounded sample of the same workload on the host cores (rank 0 only).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -397,52 +398,25 @@ def run_backward(F, dev, hbm, fp8_peak):
     return res
 
 
-def backward_only(rank):
-    """The backward-pass measurements alone (rank 0 only; no step, no baseline)."""
+def section_only(rank, section, moe_experts):
+    """One section of the other workloads alone (rank 0 only; no step, no baseline), e.g. to
+    capture its kernels with ncu. moe_experts < 256 scales the MoE workload down to that many
+    experts with the same rows per expert (tokens * experts / 256)."""
     if rank != 0:
         return None
     from fp8_fine_grained_23_b300 import fp8bs as F
     dev = torch.device("cuda", 0)
     peaks, _ = load_peaks()
-    line = {"backward": run_backward(F, dev, peaks["hbm_gbs"],
-                                     peaks["bf16_tflops"] * FP8_OVER_BF16)}
-    if F.fp8bs_last_error() != F.FP8BS_OK:
-        raise RuntimeError("a kernel reported a device-side timeout")
-    return line
+    moe_shape = WL.MOE
+    if moe_experts != WL.MOE.experts:
+        moe_shape = dataclasses.replace(
+            WL.MOE, name=f"moe_{WL.MOE.tokens * moe_experts // WL.MOE.experts}tok_{moe_experts}e_top8",
+            experts=moe_experts, tokens=WL.MOE.tokens * moe_experts // WL.MOE.experts)
+    return {"workloads": run_extras(F, dev, peaks, peaks["bf16_tflops"] * FP8_OVER_BF16,
+                                    only=section, moe_shape=moe_shape)}
 
 
-def run_ue8m0(F, dev, hbm):
-    """Power-of-two (UE8M0) tile scales against the pages' amax/448 scales on the dense
-    workload: quantizer speed, and the GEMM's relative error on a 256 x 1024 block of C against
-    the FP64 product of the BF16 inputs (computed here with PyTorch; a measurement, not parity)."""
-    a, w = WL.gemm_inputs(WL.DENSE, dev)
-    M, K = a.shape
-    N = w.shape[0]
-    res = {"workload": WL.DENSE.name}
-    ref = a[:256].double() @ w[:1024].double().t()
-    for mode, qa_fn, qw_fn in (("fp32_scales", F.fp8_quant_act_1x128, F.fp8_quant_weight_128x128),
-                               ("ue8m0_scales", F.fp8_quant_act_1x128_ue8m0,
-                                F.fp8_quant_weight_128x128_ue8m0)):
-        q = torch.empty(M, K, dtype=torch.uint8, device=dev)
-        s = torch.empty(K // 128, M, dtype=torch.float32, device=dev)
-        ms_a = _timed(lambda: qa_fn(a, q, s), dev)
-        qw = torch.empty(N, K, dtype=torch.uint8, device=dev)
-        sw = torch.empty(N // 128, K // 128, dtype=torch.float32, device=dev)
-        ms_w = _timed(lambda: qw_fn(w, qw, sw), dev)
-        c = F.fp8_blockscaled_gemm(q[:256].contiguous(), s[:, :256].contiguous(), qw[:1024],
-                                   sw[:8], out_dtype=torch.float32)
-        err = float(torch.linalg.norm(c.double() - ref) / torch.linalg.norm(ref))
-        res[mode] = {"quant_act_us": round(ms_a * 1e3, 2),
-                     "quant_act_frac_hbm": round(M * K * ACT_BYTES_PER_ELEM / (ms_a * 1e-3) / 1e9 / hbm, 4),
-                     "quant_weight_us": round(ms_w * 1e3, 2),
-                     "gemm_rel_err_vs_fp64": float(f"{err:.4g}")}
-    return res
-
-
-def run_extras(F, dev, peaks, fp8_peak):
-    out = {"timing": "each kernel alone, L2 flushed (256 MB read) before every iteration, "
-                     "mean of 10 after 3 warm-up"}
-    hbm = peaks["hbm_gbs"]
+def run_sweep(F, dev, hbm, fp8_peak):
     # quantizer bandwidth sweep
     sweep = {}
     for M in WL.SWEEP_ACT_M:
@@ -463,7 +437,10 @@ def run_extras(F, dev, peaks, fp8_peak):
                                                       "GB/s": round(gbs, 1),
                                                       "frac_hbm": round(gbs / hbm, 4)}
     del wt, q, s
-    out["quantizer_sweep"] = sweep
+    return sweep
+
+
+def run_mla(F, dev, hbm, fp8_peak):
     # MLA projections
     mla = {}
     for shape in WL.MLA:
@@ -476,7 +453,10 @@ def run_extras(F, dev, peaks, fp8_peak):
         mla[shape.name] = {"us": round(ms * 1e3, 1), "TFLOP/s": round(tf, 1),
                            "frac_fp8_peak": round(tf / fp8_peak, 4), "N_run": w.shape[0]}
         del a, w, aq, a_s, wq, w_s, c
-    out["mla_gemm"] = mla
+    return mla
+
+
+def run_decode(F, dev, hbm, fp8_peak):
     # decode-size GEMMs (few rows of A): bound by streaming the weights once
     dec = {}
     for (N, K, seed) in ((WL.DENSE.N, WL.DENSE.K, WL.DENSE.seed), (1536, 7168, 2), (24576, 1536, 4)):
@@ -491,11 +471,13 @@ def run_extras(F, dev, peaks, fp8_peak):
             dec[f"{M}x{N}x{K}"] = {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
                                    "frac_hbm": round(gbs / hbm, 4)}
         del wq, w_s, aq, a_s, c
-    out["decode_gemm"] = dec
+    return dec
+
+
+def run_moe(F, dev, hbm, fp8_peak, shape=WL.MOE):
     # MoE grouped GEMMs: gate+up and down alone (BF16 out), the gate+up GEMM with the fused
     # SwiGLU + 1x128 re-quantization, and the expert FFN chain (fused gate+up, then down on h)
     moe = {}
-    shape = WL.MOE
     off, token_of_row = WL.moe_routing(shape)
     R = int(off[-1])
     offs = torch.from_numpy(off).to(dev)
@@ -578,9 +560,29 @@ def run_extras(F, dev, peaks, fp8_peak):
                       "tokens": T, "topk": shape.topk, "N": Kh}
     del xq, xs, tok, qp, sp, rows, gw, yv, outv
     torch.cuda.empty_cache()
-    out["moe_grouped_gemm"] = moe
-    out["backward"] = run_backward(F, dev, hbm, fp8_peak)
-    out["ue8m0_variant"] = run_ue8m0(F, dev, hbm)
+    return moe
+
+
+SECTIONS = {"quantizer_sweep": run_sweep, "mla_gemm": run_mla, "decode_gemm": run_decode,
+            "moe_grouped_gemm": run_moe,
+            "backward": lambda F, dev, hbm, fp8_peak: run_backward(F, dev, hbm, fp8_peak),
+            "ue8m0_variant": lambda F, dev, hbm, fp8_peak: run_ue8m0(F, dev, hbm)}
+
+
+def run_extras(F, dev, peaks, fp8_peak, only=None, moe_shape=WL.MOE):
+    """The other configurations, each kernel timed alone; `only` runs one section."""
+    out = {"timing": "each kernel alone, L2 flushed (256 MB read) before every iteration, "
+                     "mean of 10 after 3 warm-up"}
+    hbm = peaks["hbm_gbs"]
+    for name, fn in SECTIONS.items():
+        if only is not None and name != only:
+            continue
+        if name == "moe_grouped_gemm":
+            out[name] = run_moe(F, dev, hbm, fp8_peak, moe_shape)
+            if moe_shape is not WL.MOE:
+                out[name]["reduced_workload"] = moe_shape.name
+        else:
+            out[name] = fn(F, dev, hbm, fp8_peak)
     if F.fp8bs_last_error() != F.FP8BS_OK:
         raise RuntimeError("a kernel reported a pipeline timeout in the extra workloads")
     return out
@@ -711,7 +713,13 @@ def main():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the quantizer sweep, MLA, MoE and backward workloads")
     ap.add_argument("--backward-only", action="store_true",
-                    help="time only the backward-pass kernels (one JSON object), e.g. for ncu")
+                    help="same as --only backward")
+    ap.add_argument("--only", choices=sorted(SECTIONS),
+                    help="time one section of the other workloads alone (one JSON object), "
+                         "e.g. for ncu")
+    ap.add_argument("--moe-experts", type=int, default=WL.MOE.experts,
+                    help="with --only moe_grouped_gemm: scale the MoE workload down to this "
+                         "many experts, same rows per expert (small ncu captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -723,8 +731,9 @@ def main():
             torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group(backend)
     try:
-        if args.backward_only:
-            line = backward_only(rank) if args.impl == "ours" else None
+        if args.backward_only or args.only:
+            section = args.only or "backward"
+            line = section_only(rank, section, args.moe_experts) if args.impl == "ours" else None
         elif args.impl == "reference":
             line = run_reference(args, rank, world)
         else:
