@@ -578,10 +578,32 @@ def run_moe(F, dev, hbm, fp8_peak, shape=WL.MOE):
     return moe
 
 
+def run_requant(F, dev, hbm, fp8_peak):
+    """The dense GEMM writing its output re-quantized to E4M3 with 1x128 scales (the next GEMM's
+    A operand) against the same GEMM writing BF16, each alone."""
+    a, w = WL.gemm_inputs(WL.DENSE, dev)
+    M, N, K = WL.DENSE.M, WL.DENSE.N, WL.DENSE.K
+    aq, a_s = F.fp8_quant_act_1x128(a)
+    wq, w_s = F.fp8_quant_weight_128x128(w)
+    c = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    cq = torch.empty(M, N, dtype=torch.uint8, device=dev)
+    cs = torch.empty(N // 128, M, dtype=torch.float32, device=dev)
+    res = {"workload": WL.DENSE.name}
+    for name, fn in (("bf16_out", lambda: F.fp8_blockscaled_gemm(aq, a_s, wq, w_s, out=c)),
+                     ("e4m3_1x128_out", lambda: F.fp8_blockscaled_gemm_quant(aq, a_s, wq, w_s,
+                                                                             cq, cs))):
+        ms = _timed(fn, dev)
+        tf = gemm_flops(M, N, K) / (ms * 1e-3) / 1e12
+        res[name] = {"us": round(ms * 1e3, 1), "TFLOP/s": round(tf, 1),
+                     "frac_fp8_peak": round(tf / fp8_peak, 4)}
+    return res
+
+
 SECTIONS = {"quantizer_sweep": run_sweep, "mla_gemm": run_mla, "decode_gemm": run_decode,
             "moe_grouped_gemm": run_moe,
             "backward": lambda F, dev, hbm, fp8_peak: run_backward(F, dev, hbm, fp8_peak),
-            "ue8m0_variant": lambda F, dev, hbm, fp8_peak: run_ue8m0(F, dev, hbm)}
+            "ue8m0_variant": lambda F, dev, hbm, fp8_peak: run_ue8m0(F, dev, hbm),
+            "dense_requant": run_requant}
 
 
 def run_extras(F, dev, peaks, fp8_peak, only=None, moe_shape=WL.MOE):

@@ -159,9 +159,11 @@ int check_transpose_quant_args(const void* in, int64_t rows, int64_t K, int64_t 
 // fp8_blockscaled_gemm_1d1d (per-row B scales): the same tiles, maps and persistent grid.
 int dense_gemm(GemmKind kind, const uint8_t* a_q, const float* a_s, const uint8_t* w_q,
                const float* w_s, int64_t M, int64_t N, int64_t K, void* c, int64_t ldc,
-               int out_dtype, fp8bs_stream_t stream)
+               int out_dtype, fp8bs_stream_t stream, float* c_s = nullptr)
 {
-    int st = check_gemm_args(a_q, a_s, w_q, w_s, M, N, K, c, ldc, out_dtype);
+    int st = kind == GemmKind::DENSE_QUANT ? FP8BS_OK
+                                           : check_gemm_args(a_q, a_s, w_q, w_s, M, N, K, c, ldc,
+                                                             out_dtype);
     if (st != FP8BS_OK || M == 0) return st;
     DeviceInfo* d = nullptr;
     if ((st = current_device(&d)) != FP8BS_OK) return st;
@@ -216,6 +218,7 @@ int dense_gemm(GemmKind kind, const uint8_t* a_q, const float* a_s, const uint8_
     if (items > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
     args.num_tiles = static_cast<int>(items);
     args.offsets = nullptr;
+    args.h_s = c_s;
     args.G = 1;
     args.err = d->err;
     args.budget = wait_budget();
@@ -349,6 +352,22 @@ int fp8_blockscaled_gemm_1d1d(const uint8_t* a_q, const float* a_s, const uint8_
 {
     return fp8bs::host::dense_gemm(GemmKind::ROW_SCALED, a_q, a_s, b_q, b_s, M, N, K, c, ldc,
                                    out_dtype, stream);
+}
+
+int fp8_blockscaled_gemm_quant(const uint8_t* a_q, const float* a_s, const uint8_t* w_q,
+                               const float* w_s, int64_t M, int64_t N, int64_t K, uint8_t* c_q,
+                               int64_t ldcq, float* c_s, fp8bs_stream_t stream)
+{
+    if (M < 0 || N <= 0 || N % 128 != 0 || K <= 0 || K % 128 != 0 || ldcq < N)
+        return FP8BS_ERR_INVALID_ARG;
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
+    if (M == 0) return FP8BS_OK;
+    if (!a_q || !a_s || !w_q || !w_s || !c_q || !c_s) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned16(a_q) || !aligned16(w_q) || !aligned16(c_q) || !aligned4(a_s) ||
+        !aligned4(w_s) || !aligned4(c_s) || ldcq % 16 != 0)
+        return FP8BS_ERR_MISALIGNED;
+    return fp8bs::host::dense_gemm(GemmKind::DENSE_QUANT, a_q, a_s, w_q, w_s, M, N, K, c_q, ldcq,
+                                   FP8BS_OUT_BF16, stream, c_s);
 }
 
 int fp8_quant_act_128x1(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* qt,

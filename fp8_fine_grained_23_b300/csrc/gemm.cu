@@ -227,13 +227,15 @@ __device__ __forceinline__ void st_v4(void* p, uint32_t a, uint32_t b, uint32_t 
                  : "memory");
 }
 
-template <bool GROUPED, bool OUT_F32, bool PAIR, bool RS, bool SW>
+// QO: the output re-quantized to E4M3 in 1x128 tiles (codes to p.c, scales to p.h_s).
+template <bool GROUPED, bool OUT_F32, bool PAIR, bool RS, bool SW, bool QO = false>
 __global__ void __launch_bounds__(THREADS, 1)
 fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                             const __grid_constant__ CUtensorMap map_b, const GemmArgs p)
 {
     using L = Layout<GROUPED, PAIR, RS, SW>;
     static_assert(!SW || (GROUPED && !PAIR && !RS && !OUT_F32), "SwiGLU epilogue: grouped only");
+    static_assert(!QO || (!GROUPED && !RS && !SW && !OUT_F32), "re-quantized output: dense only");
     constexpr int STAGES = L::STAGES;
     constexpr int CL = L::CL;
     extern __shared__ uint8_t smem_raw[];
@@ -596,24 +598,25 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                             ffma2(acc[8 * (c + 1) + i],
                                   fmul2(u1[i], ld_shared_u64(sb + 64 * (c + 1) + 8 * i)), sc2);
                     }
-                } else if constexpr (SW) {
-                    // gate columns 64 half .. + 63 into acc[0..31] (scale s_a * s_w[gate block]),
-                    // up columns 128 + 64 half .. + 63 into acc[32..63] (s_a * s_w[up block]);
-                    // 16-column chunks leave registers for the SwiGLU tail below
+                } else if constexpr (SW || QO) {
+                    // SW: gate columns 64 half .. + 63 into acc[0..31] (scale s_a * s_w[gate
+                    // block]), up columns 128 + 64 half .. + 63 into acc[32..63] (s_a * s_w[up
+                    // block]); QO: the usual 128 columns, one scale. 16-column chunks leave
+                    // registers for the tail that follows the K loop.
+                    auto col = [](int c) -> uint32_t {
+                        return (SW && c >= 4) ? 128 + 16 * (c - 4) : 16 * c;
+                    };
                     uint64_t u0[8], u1[8];
                     tmem_ld_16cols(taddr, u0);
 #pragma unroll
                     for (int c = 0; c < 8; c += 2) {
-                        const uint32_t col1 = (c + 1 < 4) ? 16 * (c + 1) : 128 + 16 * (c + 1 - 4);
+                        const uint32_t col1 = col(c + 1);
                         tmem_wait_ld(u0);
                         tmem_ld_16cols(taddr + col1, u1);
 #pragma unroll
                         for (int i = 0; i < 8; i++) ffma2(acc[8 * c + i], u0[i], c < 4 ? sc2 : sc2b);
                         tmem_wait_ld(u1);
-                        if (c + 2 < 8) {
-                            const uint32_t col2 = (c + 2 < 4) ? 16 * (c + 2) : 128 + 16 * (c + 2 - 4);
-                            tmem_ld_16cols(taddr + col2, u0);
-                        }
+                        if (c + 2 < 8) tmem_ld_16cols(taddr + col(c + 2), u0);
 #pragma unroll
                         for (int i = 0; i < 8; i++)
                             ffma2(acc[8 * (c + 1) + i], u1[i], c + 1 < 4 ? sc2 : sc2b);
@@ -709,6 +712,56 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                 continue;
             }
 
+            if constexpr (QO) {
+                // The output re-quantized in 1x128 tiles, the layout the next GEMM reads for its
+                // A operand: this thread's 128 columns of its row are one tile, so its amax,
+                // scale (the quantizers' tile_scale) and codes need nothing from other threads.
+                float amax = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 64; i++)
+                    amax = fmaxf(amax, fmaxf(fabsf(f32x2_lo(acc[i])), fabsf(f32x2_hi(acc[i]))));
+                const TileScale tsc = tile_scale(amax);
+                const TileInfo ts =
+                    decode_tile<GROUPED, CL>(t, p, s_tstart, s_off, static_cast<int>(crank));
+                const int col0 = ts.n0 + half * 128;            // first column of the tile
+                const int64_t grow_own = ts.row0 + r;
+                if (grow_own < ts.row_end && col0 < p.N)
+                    p.h_s[static_cast<int64_t>(col0 / 128) * p.rows + grow_own] = tsc.s;
+                const uint32_t stg = base + L::STG_OFF + (warp - EPI_WARP0) * STG_WARP_BYTES;
+                const int64_t wrow0 = ts.row0 + quad * 32;
+#pragma unroll
+                for (int g = 0; g < 2; g++) {                    // 64 codes (64 B) per round
+#pragma unroll
+                    for (int jc = 0; jc < 4; jc++) {
+                        uint32_t w4[4];
+#pragma unroll
+                        for (int e = 0; e < 4; e++) {
+                            const int q = g * 32 + jc * 8 + 2 * e;
+                            const uint32_t lo = cvt_e4m3x2(tile_scaled(f32x2_lo(acc[q]), tsc),
+                                                           tile_scaled(f32x2_hi(acc[q]), tsc));
+                            const uint32_t hi = cvt_e4m3x2(tile_scaled(f32x2_lo(acc[q + 1]), tsc),
+                                                           tile_scaled(f32x2_hi(acc[q + 1]), tsc));
+                            w4[e] = tsc.zero ? 0u : (lo | (hi << 16));
+                        }
+                        st_shared_v4(stg + lane * 64 + (((jc + (lane >> 1)) & 3) * 16),
+                                     make_uint4(w4[0], w4[1], w4[2], w4[3]));
+                    }
+                    __syncwarp();
+                    const int ch = lane & 3;
+                    const int gcol = col0 + g * 64 + ch * 16;
+#pragma unroll
+                    for (int i = 0; i < 4; i++) {
+                        const int rr = i * 8 + (lane >> 2);
+                        const uint4 v = ld_shared_v4(stg + rr * 64 + (((ch + (rr >> 1)) & 3) * 16));
+                        const int64_t grow = wrow0 + rr;
+                        if (grow < ts.row_end && gcol < p.N)
+                            st_v4(static_cast<uint8_t*>(p.c) + grow * p.ldc + gcol, v.x, v.y, v.z, v.w);
+                    }
+                    __syncwarp();
+                }
+                continue;
+            }
+
             // Store: stage this warp's 32 rows x 64 B at a time in shared memory, chunk j (16 B)
             // of row r at position (j + r/2) % 4, which keeps both the row-wise writes and the
             // column-wise reads free of bank conflicts; then write 8 rows of 64 contiguous bytes
@@ -768,16 +821,16 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     if constexpr (PAIR) cluster_sync();   // no CTA leaves while its peer still deallocates
 }
 
-template <bool GROUPED, bool OUT_F32, bool PAIR, bool RS, bool SW = false>
+template <bool GROUPED, bool OUT_F32, bool PAIR, bool RS, bool SW = false, bool QO = false>
 cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& args,
                        int max_ctas, cudaStream_t stream)
 {
     constexpr int CL = PAIR ? 2 : 1;
-    auto kern = fp8_blockscaled_gemm_kernel<GROUPED, OUT_F32, PAIR, RS, SW>;
+    auto kern = fp8_blockscaled_gemm_kernel<GROUPED, OUT_F32, PAIR, RS, SW, QO>;
     const size_t smem = gemm_smem_bytes(
         SW ? GemmKind::GROUPED_SWIGLU
            : (RS ? GemmKind::ROW_SCALED : (GROUPED ? GemmKind::GROUPED : GemmKind::DENSE)),
-        args.G);
+        args.G);   // (the re-quantized output uses the dense layout)
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -826,6 +879,7 @@ size_t gemm_smem_bytes(GemmKind kind, int G)
         return static_cast<size_t>(Layout<true, false, false, true>::GROUP_OFF) + ALIGN_PAD +
                group_table;
     case GemmKind::DENSE:
+    case GemmKind::DENSE_QUANT:
     default:
         return static_cast<size_t>(Layout<false, DENSE_PAIR, false>::GROUP_OFF) + ALIGN_PAD;
     }
@@ -843,6 +897,9 @@ cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, cons
                        : launch_one<true, false, false, false>(map_a, map_b, args, max_ctas, stream);
     case GemmKind::GROUPED_SWIGLU:
         return launch_one<true, false, false, false, true>(map_a, map_b, args, max_ctas, stream);
+    case GemmKind::DENSE_QUANT:
+        return launch_one<false, false, DP, false, false, true>(map_a, map_b, args, max_ctas,
+                                                                stream);
     case GemmKind::ROW_SCALED:
         return out_f32 ? launch_one<false, true, DP, true>(map_a, map_b, args, max_ctas, stream)
                        : launch_one<false, false, DP, true>(map_a, map_b, args, max_ctas, stream);

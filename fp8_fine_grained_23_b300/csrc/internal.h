@@ -43,7 +43,8 @@ struct GemmArgs {
     int MT;                   // dense: ceil(M / 128)
     int num_tiles;            // dense: work items = ceil(MT / cluster) * NT (grouped: on device)
     const int32_t* offsets;   // grouped: [G+1] on the device
-    float* h_s;               // GROUPED_SWIGLU: output scales [N/256][rows] (codes go to c)
+    float* h_s;               // output scales, codes go to c: GROUPED_SWIGLU [N/256][rows],
+                              // DENSE_QUANT [N/128][rows]
     int G;
     int* err;                 // device error word
     long long budget;         // spin-wait budget in SM clock cycles
@@ -96,7 +97,8 @@ cudaError_t launch_gemm_small(const CUtensorMap& map_w, const CUtensorMap& map_a
 // row and K block (the 1d1d weight-gradient GEMM), dense only.
 // GROUPED_SWIGLU: grouped, gate/up rows interleaved per 128, epilogue silu(gate) * up re-quantized
 // to E4M3 with 1x128 scales.
-enum class GemmKind { DENSE, GROUPED, ROW_SCALED, GROUPED_SWIGLU };
+// DENSE_QUANT: dense, output re-quantized to E4M3 codes with 1x128 scales.
+enum class GemmKind { DENSE, GROUPED, ROW_SCALED, GROUPED_SWIGLU, DENSE_QUANT };
 cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args,
                         GemmKind kind, bool out_f32, int max_ctas, cudaStream_t stream);
 int gemm_cluster_size(bool grouped);

@@ -38,6 +38,7 @@ lib.fp8_blockscaled_grouped_gemm_swiglu_quant.argtypes = [_p, _p, _p, _p, _p, _i
                                                          _i64, _p, _i64, _p, _p]
 lib.fp8_moe_permute.argtypes = [_p, _i64, _p, _i64, _p, _i64, _i64, _p, _i64, _p, _p]
 lib.fp8_moe_combine.argtypes = [_p, _i64, _i64, _p, _p, _i64, _i64, _i64, _p, _i64, _p]
+lib.fp8_blockscaled_gemm_quant.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, _p, _i64, _p, _p]
 lib.fp8bs_status_string.argtypes = [_int]
 lib.fp8bs_status_string.restype = ctypes.c_char_p
 lib.fp8bs_last_error.argtypes = [_p]
@@ -48,7 +49,7 @@ for _f in (lib.fp8_quant_act_1x128, lib.fp8_quant_weight_128x128, lib.fp8_blocks
            lib.fp8_quant_weight_128x128_t, lib.fp8_blockscaled_gemm_1d1d,
            lib.fp8_blockscaled_grouped_gemm_swiglu_quant, lib.fp8_moe_permute,
            lib.fp8_moe_combine, lib.fp8_quant_act_1x128_ue8m0,
-           lib.fp8_quant_weight_128x128_ue8m0):
+           lib.fp8_quant_weight_128x128_ue8m0, lib.fp8_blockscaled_gemm_quant):
     _f.restype = _int
 
 FP8BS_OK = 0
@@ -214,6 +215,25 @@ def fp8_blockscaled_gemm_1d1d(a_q: torch.Tensor, a_s: torch.Tensor, b_q: torch.T
                                          b_s.data_ptr(), M, N, K, out.data_ptr(), ldc,
                                          _out_code(out.dtype), _stream(stream)))
     return out
+
+
+def fp8_blockscaled_gemm_quant(a_q: torch.Tensor, a_s: torch.Tensor, w_q: torch.Tensor,
+                               w_s: torch.Tensor, c_q: torch.Tensor | None = None,
+                               c_s: torch.Tensor | None = None, stream=None):
+    """C = A W^T re-quantized in the epilogue: E4M3 codes c_q [M][N] and 1x128 scales
+    c_s [N/128][M] (N % 128 == 0), the layout of fp8_quant_act_1x128."""
+    M, K = a_q.shape
+    N = w_q.shape[0]
+    if c_q is None:
+        c_q = torch.empty(M, N, dtype=torch.uint8, device=a_q.device)
+    if c_s is None:
+        c_s = torch.empty(N // 128, M, dtype=torch.float32, device=a_q.device)
+    _, ldcq = _rows_ld(c_q, "c_q")
+    _check("fp8_blockscaled_gemm_quant",
+           lib.fp8_blockscaled_gemm_quant(a_q.data_ptr(), a_s.data_ptr(), w_q.data_ptr(),
+                                          w_s.data_ptr(), M, N, K, c_q.data_ptr(), ldcq,
+                                          c_s.data_ptr(), _stream(stream)))
+    return c_q, c_s
 
 
 def fp8_blockscaled_gemm_noalloc(a_q: torch.Tensor, a_s: torch.Tensor, w_q: torch.Tensor,

@@ -262,6 +262,25 @@ int fp8_blockscaled_gemm_1d1d(const uint8_t *a_q, const float *a_s,
                               void *c, int64_t ldc, int out_dtype, fp8bs_stream_t stream);
 
 /*
+ * fp8_blockscaled_gemm_quant: fp8_blockscaled_gemm with its output re-quantized to E4M3 in 1x128
+ * tiles in the epilogue, ready to be the next GEMM's A operand. The pages accumulate in higher
+ * precision and convert back to FP8 for the next computation (szhzxw.cn 一.2.c), with the
+ * scales from each tile's current maximum ([codingmall] "Định lượng trực tuyến").
+ * Per row m and 128 output columns [128 j, 128 j + 128): the FP32 results C[m][n] (accumulated
+ * exactly as fp8_blockscaled_gemm accumulates them) form one tile, quantized as
+ * fp8_quant_act_1x128 quantizes a tile (s = amax/448, codes E4M3(C * 448/amax), the same tiny
+ * and zero rules).
+ *   c_q  E4M3 codes [M][ldcq]; c_s FP32 [N/128][M] (c_s[j*M + m]).
+ * Inputs and their requirements as for fp8_blockscaled_gemm, plus N % 128 == 0, ldcq >= N,
+ * ldcq % 16 == 0, c_q 16-byte and c_s 4-byte aligned. Runs on the tiled CTA-pair kernel for
+ * every M.
+ */
+int fp8_blockscaled_gemm_quant(const uint8_t *a_q, const float *a_s,
+                               const uint8_t *w_q, const float *w_s,
+                               int64_t M, int64_t N, int64_t K,
+                               uint8_t *c_q, int64_t ldcq, float *c_s, fp8bs_stream_t stream);
+
+/*
  * fp8_blockscaled_gemm_noalloc: the same dense block-scaled GEMM as fp8_blockscaled_gemm, for
  * callers that cannot let a library allocate device memory. The pages describe no such interface;
  * this entry point has no counterpart there.

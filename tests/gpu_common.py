@@ -150,3 +150,26 @@ def oracle_grouped_swiglu_rows(aq, a_s, wq, w_s, offsets, rows):
                                                             rows[cuts[i]:cuts[i + 1]]),
                             range(len(cuts) - 1)))
     return tuple(np.concatenate([p[k] for p in parts]) for k in range(5))
+
+
+def check_requant_tiles(codes, scales, ref, delta, what):
+    """Codes [n][N] and scales [n][N/128] of an FP32 result re-quantized in 1x128 tiles, against
+    the FP64 reference `ref` [n][N] of that result with error bound `delta` [n][N]: per tile,
+    |448 s - amax(ref)| <= max delta (+ FP32 rounding), a +-448 code in every tile clearly above
+    zero, and |decode(q) s - ref| <= half an E4M3 step at the value / s, times s, + delta."""
+    from tests.helpers import e4m3_half_ulp, e4m3_values
+    n, N = ref.shape
+    T = N // 128
+    rt, dt = ref.reshape(n, T, 128), delta.reshape(n, T, 128)
+    amax = np.abs(rt).max(axis=2)
+    dmax = dt.max(axis=2)
+    s = scales.astype(np.float64)
+    bad = np.abs(448.0 * s - amax) > dmax + 2.0 ** -21 * amax + 1e-35
+    assert not bad.any(), f"{what}: {int(bad.sum())} scales outside the bound"
+    vals = e4m3_values(codes).reshape(n, T, 128)
+    live = amax > 4 * dmax
+    assert np.all(np.abs(vals).max(axis=2)[live] == 448), f"{what}: a tile without its 448 code"
+    sx = s[:, :, None]
+    bound = e4m3_half_ulp((np.abs(rt) + dt) / np.maximum(sx, 1e-300)) * sx * (1 + 2.0 ** -20) + dt + 1e-35
+    badv = np.abs(vals * sx - rt) > bound
+    assert not badv.any(), f"{what}: {int(badv.sum())} of {badv.size} values outside the bound"

@@ -29,7 +29,8 @@ def test_header_declares_the_hot_path_calls():
     for n in ("fp8_quant_act_1x128", "fp8_quant_weight_128x128", "fp8_blockscaled_gemm",
               "fp8_blockscaled_grouped_gemm", "fp8bs_status_string", "fp8bs_last_error",
               "fp8_quant_act_128x1", "fp8_quant_weight_128x128_t", "fp8_blockscaled_gemm_1d1d",
-              "fp8_blockscaled_grouped_gemm_swiglu_quant", "fp8_moe_permute", "fp8_moe_combine"):
+              "fp8_blockscaled_grouped_gemm_swiglu_quant", "fp8_moe_permute", "fp8_moe_combine",
+              "fp8_blockscaled_gemm_quant"):
         assert n in names
 
 
@@ -149,6 +150,16 @@ def test_moe_dispatch_argument_checks(F):
     assert cm(P16, 64, 8, P4, P4, 4, 8, 60, P16, 64, None) == -1                  # N % 8
     assert cm(P16, 68, 8, P4, P4, 4, 8, 64, P16, 64, None) == -2                  # ldy % 8
     assert cm(P16 + 4, 64, 8, P4, P4, 4, 8, 64, P16, 64, None) == -2              # y alignment
+
+
+def test_gemm_quant_argument_checks(F):
+    g = F.lib.fp8_blockscaled_gemm_quant
+    assert g(P16, P4, P16, P4, 0, 256, 128, P16, 256, P4, None) == 0      # M == 0
+    assert g(P16, P4, P16, P4, 4, 192, 128, P16, 256, P4, None) == -1     # N % 128
+    assert g(P16, P4, P16, P4, 4, 256, 128, P16, 128, P4, None) == -1     # ldcq < N
+    assert g(P16, P4, P16, P4, 4, 256, 128, P16, 264, P4, None) == -2     # ldcq % 16
+    assert g(P16, P4, P16, P4, 4, 256, 128, P16 + 1, 256, P4, None) == -2 # c_q alignment
+    assert g(P16, P4, P16, P4, 4, 256, 128, P16, 256, None, None) == -1   # no c_s
 
 
 def test_debug_hook_rejects_negative_index(F):
