@@ -20,6 +20,7 @@
 //              and its two weight-block scales into an 8-slot shared-memory ring (sfull/sempty
 //              mbarriers), so the epilogue reads its scale from shared memory;
 //   warp 3     idle after set-up (warp 0 also builds the group table of the grouped variant);
+//              the grouped variant's tiles follow the group table built from device offsets;
 //   warps 4-11 epilogue: warp w reads TMEM lanes 32*(w%4).. (its rows) and the 128 columns
 //              128*((w-4)/4).. (one weight block). Per K block it loads the partial in 32-column
 //              pieces (the next piece in flight while the current one is promoted) and promotes
@@ -36,6 +37,17 @@
 // forwards each release to the even CTA's `tempty`, keeping the slow cross-CTA arrive off the
 // epilogue's path. The grouped GEMM, which is bound
 // by streaming expert weights from HBM, keeps single-CTA MMAs on 128x256 tiles.
+//
+// Variants of the same kernel (template flags):
+//   RS   (dense) B carries a scale per row and K block (the backward weight-gradient GEMM):
+//        the scale ring holds the tile's 256 B-row scales and the promotion is
+//        acc = fma(P * s_b[n], s_a[m], acc), in 16-column TMEM chunks;
+//   SW   (grouped) gate and up weight rows interleaved per 128: a thread promotes 64 gate and the
+//        matching 64 up columns, forms silu(gate) * up, exchanges row maxima with the partner
+//        warp of its lane quarter and stores E4M3 codes with 1x128 scales;
+//   QO   (dense) the output re-quantized to E4M3 in 1x128 tiles: a thread's 128 columns are one
+//        tile, so amax, scale and codes are thread-local.
+// (Few rows of A, M <= 64, go to the swap-AB kernel in gemm_small.cu instead.)
 //
 // Registers: the launch gives 168 per thread (65536 / 384, rounded to 8). Warpgroup 0 drops to
 // 72 and the two epilogue warpgroups rise to 216 (128*72 + 256*216 = 384*168), which holds the
