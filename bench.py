@@ -599,8 +599,41 @@ def run_requant(F, dev, hbm, fp8_peak):
     return res
 
 
+def run_library_reference(F, dev, hbm, fp8_peak):
+    """A library FP8 GEMM on the dense shape as the external comparison point: cuBLASLt through
+    torch._scaled_mm with one scale per tensor (no per-block scales, so no promotion work; an
+    upper bound for the block-scaled kernel on the same codes). The block-scaled library form
+    (1x128 x 128x128 scales) is tried too and its answer recorded."""
+    a, w = WL.gemm_inputs(WL.DENSE, dev)
+    M, N, K = WL.DENSE.M, WL.DENSE.N, WL.DENSE.K
+    aq, a_s = F.fp8_quant_act_1x128(a)
+    wq, w_s = F.fp8_quant_weight_128x128(w)
+    a8, w8t = aq.view(torch.float8_e4m3fn), wq.view(torch.float8_e4m3fn).t()
+    one = torch.ones((), dtype=torch.float32, device=dev)
+    c = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    res = {"workload": WL.DENSE.name, "library": f"cuBLASLt (torch {torch.__version__})"}
+    runs = (("ours_block_scaled", lambda: F.fp8_blockscaled_gemm(aq, a_s, wq, w_s, out=c)),
+            ("cublaslt_per_tensor_fp8",
+             lambda: torch._scaled_mm(a8, w8t, one, one, out_dtype=torch.bfloat16)))
+    for name, fn in runs:
+        ms = _timed(fn, dev)
+        tf = gemm_flops(M, N, K) / (ms * 1e-3) / 1e12
+        res[name] = {"us": round(ms * 1e3, 1), "TFLOP/s": round(tf, 1),
+                     "frac_fp8_peak": round(tf / fp8_peak, 4)}
+    res["ours_over_library"] = round(res["cublaslt_per_tensor_fp8"]["us"] /
+                                     res["ours_block_scaled"]["us"], 4)
+    try:
+        from torch.nn.functional import ScalingType, scaled_mm
+        scaled_mm(a8, w8t, a_s.t(), ScalingType.BlockWise1x128, w_s.t(),
+                  ScalingType.BlockWise128x128, output_dtype=torch.bfloat16)
+        res["library_block_scaled"] = "ran (not timed)"
+    except Exception as e:   # not offered on this GPU: record the library's own answer
+        res["library_block_scaled"] = f"unavailable: {type(e).__name__}: {str(e)[:160]}"
+    return res
+
+
 SECTIONS = {"quantizer_sweep": run_sweep, "mla_gemm": run_mla, "decode_gemm": run_decode,
-            "moe_grouped_gemm": run_moe,
+            "moe_grouped_gemm": run_moe, "library_reference": run_library_reference,
             "backward": lambda F, dev, hbm, fp8_peak: run_backward(F, dev, hbm, fp8_peak),
             "ue8m0_variant": lambda F, dev, hbm, fp8_peak: run_ue8m0(F, dev, hbm),
             "dense_requant": run_requant}
