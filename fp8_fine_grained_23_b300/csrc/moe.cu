@@ -82,9 +82,10 @@ moe_combine_kernel(const uint16_t* __restrict__ y, int64_t ldy, int64_t R,
         my_row = (rv >= 0 && rv < R) ? rv : -1;
         my_w = w[t * topk + lane];
     }
-    // A warp step covers 2 KB of every row it reads (lane l: 16-byte chunks 4 l .. 4 l + 3 of
-    // the step), so the gathered rows reach DRAM in long runs; rows go 4 at a time, their loads
-    // issued before their fma chains.
+    // A warp step covers 2 KB of every row it reads (lane l: 16-byte chunks l, l + 32, l + 64,
+    // l + 96 of the step, so that each load instruction reads 512 contiguous bytes), and the
+    // gathered rows reach DRAM in long runs; rows go 4 at a time, their loads issued before their
+    // fma chains.
     const int chunks = N / 8;
     for (int c0 = 0; c0 < chunks; c0 += 128) {
         float acc[4][8];
@@ -103,7 +104,7 @@ moe_combine_kernel(const uint16_t* __restrict__ y, int64_t ldy, int64_t R,
                 wj[jj] = use ? __shfl_sync(0xffffffffu, my_w, j & 31) : 0.0f;
 #pragma unroll
                 for (int q = 0; q < 4; q++) {
-                    const int c = c0 + 4 * lane + q;
+                    const int c = c0 + lane + 32 * q;
                     v[jj][q] = (use && c < chunks) ? ld_nc_v4(y + rj * ldy + 8 * c)
                                                    : make_uint4(0, 0, 0, 0);
                 }
@@ -126,7 +127,7 @@ moe_combine_kernel(const uint16_t* __restrict__ y, int64_t ldy, int64_t R,
         }
 #pragma unroll
         for (int q = 0; q < 4; q++) {
-            const int c = c0 + 4 * lane + q;
+            const int c = c0 + lane + 32 * q;
             if (c >= chunks) continue;
             uint32_t o[4];
 #pragma unroll
