@@ -32,10 +32,13 @@
 // tile with one 256-row MMA per K step, issued by the even CTA. Each CTA loads only its own 128
 // A rows and 128 of the 256 W rows, so a K block brings 32 KB into each SM instead of 48 KB, and
 // a stage takes 32 KB, which leaves room for six. Both CTAs' loads complete on the even CTA's
-// `full` barrier; the MMA commits are multicast to both CTAs' `empty` and `tfull` barriers. Each
-// CTA's epilogue releases its local `tempty` barrier; the odd CTA's MMA warp, otherwise idle,
-// forwards each release to the even CTA's `tempty`, keeping the slow cross-CTA arrive off the
-// epilogue's path. The grouped GEMM, which is bound
+// `full` barrier; the MMA commits are multicast to both CTAs' `empty` and `tfull` barriers. The
+// epilogue warps of both CTAs release a TMEM buffer on the even CTA's `tempty` barrier (the odd
+// CTA's by remote arrives; in the row-scaled and re-quantizing variants, whose epilogues have no
+// register to spare, the odd CTA's otherwise idle MMA warp forwards its local release instead).
+// The per-K-block hand-over of the partial through TMEM is what bounds this kernel: two buffers
+// hold 1024 MMA cycles, less than the chain MMA completion -> drain -> release -> next MMA.
+// The grouped GEMM, which is bound
 // by streaming expert weights from HBM, keeps single-CTA MMAs on 128x256 tiles.
 //
 // Variants of the same kernel (template flags):
@@ -250,6 +253,10 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     static_assert(!QO || (!GROUPED && !RS && !SW && !OUT_F32), "re-quantized output: dense only");
     constexpr int STAGES = L::STAGES;
     constexpr int CL = L::CL;
+    // Odd-CTA epilogue warps release TMEM straight to the even CTA (2% faster than forwarding
+    // through the odd CTA's MMA warp); the row-scaled and re-quantizing epilogues keep the
+    // forwarding, which costs them no registers.
+    constexpr bool DIRECT_RELEASE = PAIR && !RS && !QO;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + (ALIGN_PAD - 1)) & ~static_cast<uint32_t>(ALIGN_PAD - 1);
@@ -287,8 +294,10 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
         }
         for (int b = 0; b < 2; b++) {
             mbar_init(tfull0 + 8 * b, 1);
-            // local epilogue warps, plus (even CTA of a pair) one forwarded arrive from the peer
-            mbar_init(tempty0 + 8 * b, NUM_EPI_WARPS + ((PAIR && leader) ? 1 : 0));
+            // the local epilogue warps, plus (even CTA of a pair) the odd CTA's: its epilogue
+            // warps' own remote arrives, or one forwarded arrive
+            mbar_init(tempty0 + 8 * b,
+                      NUM_EPI_WARPS + ((PAIR && leader) ? (DIRECT_RELEASE ? NUM_EPI_WARPS : 1) : 0));
         }
         mbar_init(drain_bar, 1);
         for (int i = 0; i < SCALE_SLOTS; i++) {
@@ -448,8 +457,9 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                         mma_commit(drain_bar);
                     if (!mbar_wait(drain_bar, 0, 0u, budget)) atomicCAS(p.err, 0, DEV_TIMEOUT_DRAIN);
                 }
-            } else if (PAIR && !leader && lane == 0) {
-                // Odd CTA of a pair: forward the release of each TMEM accumulator by this CTA's
+            } else if (PAIR && !DIRECT_RELEASE && !leader && lane == 0) {
+                // Odd CTA of a pair (variants whose epilogue has no register to spare for the
+                // remote release): forward the release of each TMEM accumulator by this CTA's
                 // epilogue (its local tempty barrier) to the even CTA, whose MMA waits for both.
                 const uint32_t peer_tempty0 = mapa_shared(tempty0, crank & ~1u);
                 uint32_t j = 0;
@@ -658,8 +668,15 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     if (lane == 0) mbar_arrive(sempty0 + 8 * slot);
                 }
                 // (test hook: one epilogue warp can be told to skip one release, see GemmArgs)
-                if (lane == 0 && !(warp == EPI_WARP0 && static_cast<int>(j) == p.fault_skip_release))
-                    mbar_arrive(tempty0 + 8 * b);
+                // A pair's MMAs write both CTAs' TMEM: the odd CTA's warps release their half of
+                // the buffer on the even CTA's barrier with a plain remote arrive (the TMEM reads
+                // are already ordered by tcgen05.wait::ld and the fence above).
+                if (lane == 0 && !(warp == EPI_WARP0 && static_cast<int>(j) == p.fault_skip_release)) {
+                    if (DIRECT_RELEASE && !leader)
+                        mbar_arrive_cluster(mapa_shared(tempty0 + 8 * b, crank & ~1u));
+                    else
+                        mbar_arrive(tempty0 + 8 * b);
+                }
             }
             if (!ok) break;
 
