@@ -578,6 +578,34 @@ def run_moe(F, dev, hbm, fp8_peak, shape=WL.MOE):
     return moe
 
 
+def run_ue8m0(F, dev, hbm):
+    """Power-of-two (UE8M0) tile scales against the pages' amax/448 scales on the dense
+    workload: quantizer speed, and the GEMM's relative error on a 256 x 1024 block of C against
+    the FP64 product of the BF16 inputs (computed here with PyTorch; a measurement, not parity)."""
+    a, w = WL.gemm_inputs(WL.DENSE, dev)
+    M, K = a.shape
+    N = w.shape[0]
+    res = {"workload": WL.DENSE.name}
+    ref = a[:256].double() @ w[:1024].double().t()
+    for mode, qa_fn, qw_fn in (("fp32_scales", F.fp8_quant_act_1x128, F.fp8_quant_weight_128x128),
+                               ("ue8m0_scales", F.fp8_quant_act_1x128_ue8m0,
+                                F.fp8_quant_weight_128x128_ue8m0)):
+        q = torch.empty(M, K, dtype=torch.uint8, device=dev)
+        s = torch.empty(K // 128, M, dtype=torch.float32, device=dev)
+        ms_a = _timed(lambda: qa_fn(a, q, s), dev)
+        qw = torch.empty(N, K, dtype=torch.uint8, device=dev)
+        sw = torch.empty(N // 128, K // 128, dtype=torch.float32, device=dev)
+        ms_w = _timed(lambda: qw_fn(w, qw, sw), dev)
+        c = F.fp8_blockscaled_gemm(q[:256].contiguous(), s[:, :256].contiguous(), qw[:1024],
+                                   sw[:8], out_dtype=torch.float32)
+        err = float(torch.linalg.norm(c.double() - ref) / torch.linalg.norm(ref))
+        res[mode] = {"quant_act_us": round(ms_a * 1e3, 2),
+                     "quant_act_frac_hbm": round(M * K * ACT_BYTES_PER_ELEM / (ms_a * 1e-3) / 1e9 / hbm, 4),
+                     "quant_weight_us": round(ms_w * 1e3, 2),
+                     "gemm_rel_err_vs_fp64": float(f"{err:.4g}")}
+    return res
+
+
 def run_requant(F, dev, hbm, fp8_peak):
     """The dense GEMM writing its output re-quantized to E4M3 with 1x128 scales (the next GEMM's
     A operand) against the same GEMM writing BF16, each alone."""
