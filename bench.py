@@ -670,17 +670,22 @@ SECTIONS = {"quantizer_sweep": run_sweep, "mla_gemm": run_mla, "decode_gemm": ru
 def run_extras(F, dev, peaks, fp8_peak, only=None, moe_shape=WL.MOE):
     """The other configurations, each kernel timed alone; `only` runs one section."""
     out = {"timing": "each kernel alone, L2 flushed (256 MB read) before every iteration, "
-                     "mean of 10 after 3 warm-up"}
+                     "mean of 10 after 3 warm-up; a 1 s pause before each section, whose SM "
+                     "clocks are sampled while it runs"}
     hbm = peaks["hbm_gbs"]
     for name, fn in SECTIONS.items():
         if only is not None and name != only:
             continue
+        time.sleep(1.0)   # let the power state of the previous section settle
+        sampler = ClockSampler(dev.index if dev.index is not None else 0)
+        sampler.start()
         if name == "moe_grouped_gemm":
             out[name] = run_moe(F, dev, hbm, fp8_peak, moe_shape)
             if moe_shape is not WL.MOE:
                 out[name]["reduced_workload"] = moe_shape.name
         else:
             out[name] = fn(F, dev, hbm, fp8_peak)
+        out[name]["clocks"] = sampler.stop()
     if F.fp8bs_last_error() != F.FP8BS_OK:
         raise RuntimeError("a kernel reported a pipeline timeout in the extra workloads")
     return out
