@@ -34,8 +34,8 @@
 // a stage takes 32 KB, which leaves room for six. Both CTAs' loads complete on the even CTA's
 // `full` barrier; the MMA commits are multicast to both CTAs' `empty` and `tfull` barriers. The
 // epilogue warps of both CTAs release a TMEM buffer on the even CTA's `tempty` barrier (the odd
-// CTA's by remote arrives; in the row-scaled and re-quantizing variants, whose epilogues have no
-// register to spare, the odd CTA's otherwise idle MMA warp forwards its local release instead).
+// CTA's by remote arrives; in the row-scaled variant, whose epilogue has no register to spare,
+// the odd CTA's otherwise idle MMA warp forwards its local release instead).
 // The per-K-block hand-over of the partial through TMEM is what bounds this kernel: two buffers
 // hold 1024 MMA cycles, less than the chain MMA completion -> drain -> release -> next MMA.
 // The grouped GEMM, which is bound
@@ -254,9 +254,9 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     constexpr int STAGES = L::STAGES;
     constexpr int CL = L::CL;
     // Odd-CTA epilogue warps release TMEM straight to the even CTA (2% faster than forwarding
-    // through the odd CTA's MMA warp); the row-scaled and re-quantizing epilogues keep the
-    // forwarding, which costs them no registers.
-    constexpr bool DIRECT_RELEASE = PAIR && !RS && !QO;
+    // through the odd CTA's MMA warp); the row-scaled epilogue keeps the forwarding, which costs
+    // it no registers (the remote address spills there).
+    constexpr bool DIRECT_RELEASE = PAIR && !RS;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + (ALIGN_PAD - 1)) & ~static_cast<uint32_t>(ALIGN_PAD - 1);
@@ -546,6 +546,8 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                                                      // gate 64*half.. + 63 and up 128 + 64*half..)
         const int r = quad * 32 + lane;              // row within the tile
         const uint32_t t_lane = static_cast<uint32_t>(quad * 32) << 16;
+        // the even CTA's tempty barriers as cluster addresses (QO's form of the remote release)
+        const uint32_t release0 = PAIR ? mapa_shared(tempty0, crank & ~1u) : tempty0;
         uint32_t j = 0;
         uint64_t acc[64];   // 128 FP32 accumulators as packed pairs (columns 2i, 2i + 1)
         uint32_t tile_n = 0;   // tiles finished by this CTA (SW: parity of the exchange buffers)
@@ -672,7 +674,11 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                 // the buffer on the even CTA's barrier with a plain remote arrive (the TMEM reads
                 // are already ordered by tcgen05.wait::ld and the fence above).
                 if (lane == 0 && !(warp == EPI_WARP0 && static_cast<int>(j) == p.fault_skip_release)) {
-                    if (DIRECT_RELEASE && !leader)
+                    // (the two forms of the remote arrive are the ones that fit each variant's
+                    // registers without spilling)
+                    if constexpr (DIRECT_RELEASE && QO)
+                        mbar_arrive_cluster(release0 + 8 * b);
+                    else if (DIRECT_RELEASE && !leader)
                         mbar_arrive_cluster(mapa_shared(tempty0 + 8 * b, crank & ~1u));
                     else
                         mbar_arrive(tempty0 + 8 * b);
