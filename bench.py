@@ -83,10 +83,14 @@ class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # the extras' sampler also records the memory clock and the HBM temperature
+    MEMORY_FIELDS = ",clocks.mem,temperature.memory"
 
-    def __init__(self, device_index: int):
+    def __init__(self, device_index: int, memory: bool = False):
         self.proc = None
         self.path = None
+        self.memory = memory
+        self.n_fields = 10 if memory else 8
         try:
             uuid = str(torch.cuda.get_device_properties(device_index).uuid)
             self.ident = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
@@ -98,7 +102,8 @@ class ClockSampler:
         os.close(fd)
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", self.ident, f"--query-gpu={self.FIELDS}",
+                ["nvidia-smi", "-i", self.ident,
+                 f"--query-gpu={self.FIELDS + (self.MEMORY_FIELDS if self.memory else '')}",
                  "--format=csv,noheader,nounits", "-lms", "100", "-f", self.path],
                 stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
         except OSError:
@@ -116,7 +121,7 @@ class ClockSampler:
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) == 8:
+                if len(parts) == self.n_fields:
                     rows.append(parts)
         os.unlink(self.path)
         if not rows:
@@ -132,9 +137,14 @@ class ClockSampler:
         mx = [num(r[1]) for r in rows]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i] == "Active"})
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "power_w_max": max(num(r[2]) for r in rows), "samples": len(rows),
-                "reasons": reasons}
+        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+               "power_w_max": max(num(r[2]) for r in rows), "samples": len(rows),
+               "reasons": reasons}
+        if self.memory:
+            out["mem_mhz_min"] = min(num(r[8]) for r in rows)
+            out["hbm_temp_c_max"] = max(num(r[9]) for r in rows)
+        # a field the GPU does not report ("N/A") becomes null, never NaN, in the JSON line
+        return {k: (None if isinstance(v, float) and v != v else v) for k, v in out.items()}
 
 
 # --------------------------------------------------------------------------------------
@@ -677,7 +687,7 @@ def run_extras(F, dev, peaks, fp8_peak, only=None, moe_shape=WL.MOE):
         if only is not None and name != only:
             continue
         time.sleep(1.0)   # let the power state of the previous section settle
-        sampler = ClockSampler(dev.index if dev.index is not None else 0)
+        sampler = ClockSampler(dev.index if dev.index is not None else 0, memory=True)
         sampler.start()
         if name == "moe_grouped_gemm":
             out[name] = run_moe(F, dev, hbm, fp8_peak, moe_shape)
