@@ -365,20 +365,22 @@ def run_ours(args, rank, world, local_rank):
 def _timed(fn, dev, iters=10, warm=3):
     """Mean device time (ms) of fn(). Before every run L2 is flushed by reading a 256 MB buffer
     (written once up front): reading evicts the cache without leaving dirty lines whose
-    write-back would then compete with the kernel being timed."""
+    write-back would then compete with the kernel being timed. A spin kernel queued first keeps
+    the GPU busy while the host enqueues every iteration, so that no host launch gap can fall
+    between an iteration's start event and its kernel."""
     flush = torch.ones(64 * 1024 * 1024, dtype=torch.float32, device=dev)   # 256 MB
     stream = torch.cuda.current_stream(dev)
-    times = []
-    for i in range(warm + iters):
+    events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(warm + iters)]
+    torch.cuda.synchronize(dev)
+    torch.cuda._sleep(400_000 * (warm + iters))   # ~0.2 ms of GPU clock cycles per iteration
+    for e0, e1 in events:
         sink = flush.sum()   # noqa: F841  (read-only flush)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         fn()
         e1.record(stream)
-        if i >= warm:
-            times.append((e0, e1))
     torch.cuda.synchronize(dev)
-    return statistics.mean(a.elapsed_time(b) for a, b in times)
+    return statistics.mean(a.elapsed_time(b) for a, b in events[warm:])
 
 
 def run_backward(F, dev, hbm, fp8_peak):
@@ -680,8 +682,9 @@ SECTIONS = {"quantizer_sweep": run_sweep, "mla_gemm": run_mla, "decode_gemm": ru
 def run_extras(F, dev, peaks, fp8_peak, only=None, moe_shape=WL.MOE):
     """The other configurations, each kernel timed alone; `only` runs one section."""
     out = {"timing": "each kernel alone, L2 flushed (256 MB read) before every iteration, "
-                     "mean of 10 after 3 warm-up; a 1 s pause before each section, whose SM "
-                     "clocks are sampled while it runs"}
+                     "mean of 10 after 3 warm-up, all enqueued behind a GPU spin so that no host "
+                     "launch gap is timed; a 1 s pause before each section, whose SM clocks are "
+                     "sampled while it runs"}
     hbm = peaks["hbm_gbs"]
     for name, fn in SECTIONS.items():
         if only is not None and name != only:
