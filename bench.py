@@ -683,13 +683,11 @@ def run_extras(F, dev, peaks, fp8_peak, only=None, moe_shape=WL.MOE):
     """The other configurations, each kernel timed alone; `only` runs one section."""
     out = {"timing": "each kernel alone, L2 flushed (256 MB read) before every iteration, "
                      "mean of 10 after 3 warm-up, all enqueued behind a GPU spin so that no host "
-                     "launch gap is timed; a 1 s pause before each section, whose SM clocks are "
-                     "sampled while it runs"}
+                     "launch gap is timed; SM and memory clocks sampled during each section"}
     hbm = peaks["hbm_gbs"]
     for name, fn in SECTIONS.items():
         if only is not None and name != only:
             continue
-        time.sleep(1.0)   # let the power state of the previous section settle
         sampler = ClockSampler(dev.index if dev.index is not None else 0, memory=True)
         sampler.start()
         if name == "moe_grouped_gemm":
