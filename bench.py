@@ -373,7 +373,7 @@ def _timed(fn, dev, iters=10, warm=3):
     events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(warm + iters)]
     torch.cuda.synchronize(dev)
-    torch.cuda._sleep(400_000 * (warm + iters))   # ~0.2 ms of GPU clock cycles per iteration
+    torch.cuda._sleep(250_000 * (warm + iters))   # ~0.12 ms of GPU clock cycles per iteration
     for e0, e1 in events:
         sink = flush.sum()   # noqa: F841  (read-only flush)
         e0.record(stream)
