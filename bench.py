@@ -761,18 +761,23 @@ def _calibrate_rows(a_bits, w_bits, threads, budget_s):
     return max(1, min(SHAPE.M, rows))
 
 
-def cpu_baseline(budget_s: float = 20.0):
+def cpu_baseline(budget_s: float = 20.0, single_core_budget_s: float = 8.0):
+    """The oracle on all host cores (the reported baseline) and, beside it, on one core."""
     a_bits, w_bits = _host_inputs()
     threads = _threads()
     N, K = SHAPE.N, SHAPE.K
     rows = _calibrate_rows(a_bits, w_bits, threads, budget_s)
     t = _oracle_sample(rows, a_bits, w_bits, threads)
     value = gemm_flops(rows, N, K) / t / 1e12
+    rows1 = _calibrate_rows(a_bits, w_bits, 1, single_core_budget_s)
+    t1 = _oracle_sample(rows1, a_bits, w_bits, 1)
     return {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "seconds": round(t, 3),
             "sample": f"oracle step on {rows} of {SHAPE.M} activation rows: quantize those rows "
                       f"and all of W ({N}x{K}), then the FP64 block-scaled GEMM of the "
-                      f"{rows}x{N}x{K} slab; value = 2*{rows}*{N}*{K} / wall time"}
+                      f"{rows}x{N}x{K} slab; value = 2*{rows}*{N}*{K} / wall time",
+            "single_core": {"value": gemm_flops(rows1, N, K) / t1 / 1e12, "rows": rows1,
+                            "seconds": round(t1, 3)}}
 
 
 def run_reference(args, rank, world):
