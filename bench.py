@@ -362,8 +362,8 @@ def run_ours(args, rank, world, local_rank):
 # The other workloads, each kernel timed alone (L2 flushed between iterations)
 # --------------------------------------------------------------------------------------
 
-def _timed(fn, dev, iters=50, warm=5):
-    """Median device time (ms) of fn(). Before every run L2 is flushed by reading a 256 MB buffer
+def _timed(fn, dev, iters=10, warm=3):
+    """Mean device time (ms) of fn(). Before every run L2 is flushed by reading a 256 MB buffer
     (written once up front): reading evicts the cache without leaving dirty lines whose
     write-back would then compete with the kernel being timed. A spin kernel queued first keeps
     the GPU busy while the host enqueues every iteration, so that no host launch gap can fall
@@ -380,7 +380,7 @@ def _timed(fn, dev, iters=50, warm=5):
         fn()
         e1.record(stream)
     torch.cuda.synchronize(dev)
-    return statistics.median(a.elapsed_time(b) for a, b in events[warm:])
+    return statistics.mean(a.elapsed_time(b) for a, b in events[warm:])
 
 
 def run_backward(F, dev, hbm, fp8_peak):
@@ -682,7 +682,7 @@ SECTIONS = {"quantizer_sweep": run_sweep, "mla_gemm": run_mla, "decode_gemm": ru
 def run_extras(F, dev, peaks, fp8_peak, only=None, moe_shape=WL.MOE):
     """The other configurations, each kernel timed alone; `only` runs one section."""
     out = {"timing": "each kernel alone, L2 flushed (256 MB read) before every iteration, "
-                     "median of 50 after 5 warm-up, all enqueued behind a GPU spin so that no host "
+                     "mean of 10 after 3 warm-up, all enqueued behind a GPU spin so that no host "
                      "launch gap is timed; SM and memory clocks sampled during each section"}
     hbm = peaks["hbm_gbs"]
     for name, fn in SECTIONS.items():
