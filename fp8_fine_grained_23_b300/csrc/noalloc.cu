@@ -3,10 +3,10 @@
 //
 // The GEMM kernel needs one word of global scratch: the error word in which a CTA records a
 // pipeline wait that ran past its budget. fp8_blockscaled_gemm obtains that word with cudaMalloc on
-// its first call on a device. Some callers cannot let a library allocate: code that runs while a
-// CUDA graph is being captured in a mode that forbids allocation, runtimes that hand out all device
-// memory through their own pool and forbid any other cudaMalloc, and embedded deployments that
-// must know their full device footprint before they start. This entry point runs the same kernel
+// its first call on a device. Some callers cannot let a library allocate: frameworks that hand
+// out all device memory through their own caching allocator or pool and treat any other cudaMalloc
+// as an error (it would fragment or overrun the pool's budget), and deployments that must know
+// their full device footprint before they start. This entry point runs the same kernel
 // with its scratch in a fixed array that lives in the library image itself (a static __device__
 // array, loaded on every GPU that loads the library and kept until the process exits). Nothing is
 // allocated per call or on the first call.

@@ -285,11 +285,11 @@ int fp8_blockscaled_gemm_quant(const uint8_t *a_q, const float *a_s,
  * callers that cannot let a library allocate device memory. The pages describe no such interface;
  * this entry point has no counterpart there.
  *
- * Who needs it: code that runs while a CUDA graph is captured in a mode that forbids allocation,
- * runtimes that own all device memory through their own pool and forbid other cudaMalloc calls,
- * and deployments that must fix their device footprint before they start. fp8_blockscaled_gemm
- * allocates a 4-byte error word with cudaMalloc on its first call on a device; this variant never
- * calls cudaMalloc, cudaFree or any allocating routine.
+ * Who needs it: frameworks that hand out all device memory through their own caching allocator
+ * or pool and treat any cudaMalloc behind its back as an error (it would fragment or exceed the
+ * pool's budget), and deployments that must fix their device footprint before they start.
+ * fp8_blockscaled_gemm allocates a 4-byte error word with cudaMalloc on its first call on a
+ * device; this variant never calls cudaMalloc, cudaFree or any allocating routine.
  *
  * Instead its kernel keeps that scratch word in a fixed 256-byte array inside the library image
  * (a static __device__ array: every GPU that loads the library holds it until the process exits).

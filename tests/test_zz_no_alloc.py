@@ -1,7 +1,8 @@
 """The allocation-free GEMM entry point (fp8_blockscaled_gemm_noalloc) against the regular one.
 
-Some callers cannot let the library allocate device memory (allocation-free graph capture, a
-runtime that owns all device memory, a fixed device footprint). For them the library runs the
+Some callers cannot let the library allocate device memory: a framework whose own caching
+allocator or pool must be the only source of device memory, or a deployment whose device
+footprint is fixed before it starts. For them the library runs the
 dense GEMM with its scratch word in a fixed array inside its own image. This test calls that
 entry point through the C ABI twice in a row (the second call reuses the scratch the first call
 left behind) and checks both outputs against fp8_blockscaled_gemm's, within the GEMM tolerance
