@@ -750,10 +750,11 @@ def _threads():
 
 def _calibrate_rows(a_bits, w_bits, threads, budget_s):
     """Rows of the oracle sample that take about budget_s seconds: two probes give the fixed
-    cost (quantizing W) and the cost per activation row."""
-    r1 = threads
+    cost (quantizing W) and the cost per activation row. The probes differ by at least 16 rows,
+    so that the per-row cost stands out of the run-to-run noise of the fixed cost."""
+    r1 = max(threads, 4)
     t1 = _oracle_sample(r1, a_bits, w_bits, threads)
-    r2 = 3 * threads
+    r2 = r1 + max(2 * threads, 16)
     t2 = _oracle_sample(r2, a_bits, w_bits, threads)
     per_row = max((t2 - t1) / (r2 - r1), 1e-6)
     fixed = max(t1 - r1 * per_row, 0.0)
