@@ -2,12 +2,13 @@
 
 Some callers cannot let the library allocate device memory: a framework whose own caching
 allocator or pool must be the only source of device memory, or a deployment whose device
-footprint is fixed before it starts. For them the library runs the
-dense GEMM with its scratch word in a fixed array inside its own image. This test calls that
-entry point through the C ABI twice in a row (the second call reuses the scratch the first call
-left behind) and checks both outputs against fp8_blockscaled_gemm's, within the GEMM tolerance
-the other tests use (they are in fact identical: same kernel, same arithmetic). The file is named
-to be collected last and passes alone in a fresh process as well as after the other tests.
+footprint is fixed before it starts. For them the library runs the dense GEMM with its scratch
+word in a fixed array inside its own image. This test calls that entry point through the C ABI
+twice in a row (the second call reuses the scratch the first call left behind), on the tiny
+workload and on a ragged shape, and checks both outputs against fp8_blockscaled_gemm's, within
+the GEMM tolerance the other tests use (they are in fact identical: same kernel, same
+arithmetic). The file is named to be collected last and passes alone in a fresh process as well
+as after the other tests.
 """
 import numpy as np
 import pytest
@@ -21,9 +22,19 @@ from tests.helpers import bits_of
 pytestmark = pytest.mark.gpu
 
 
+def _ragged_inputs(M, N, K, seed):
+    g = W.generator(seed, "cpu")
+    return W.activations(M, K, g, "cpu"), W.weights(N, K, g, "cpu")
+
+
+@pytest.mark.parametrize("shape", ["tiny", "200x272x384"])
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
-def test_noalloc_gemm_matches_regular_entry_point(F, out_dtype):
-    a, w = W.gemm_inputs(W.TINY, "cpu")
+def test_noalloc_gemm_matches_regular_entry_point(F, out_dtype, shape):
+    if shape == "tiny":
+        a, w = W.gemm_inputs(W.TINY, "cpu")
+    else:
+        M, N, K = (int(v) for v in shape.split("x"))
+        a, w = _ragged_inputs(M, N, K, seed=M + N)
     M, K = a.shape
     N = w.shape[0]
     aq, a_s = F.fp8_quant_act_1x128(a.cuda())
@@ -48,7 +59,7 @@ def test_noalloc_gemm_matches_regular_entry_point(F, out_dtype):
         got = out.float().cpu().numpy().astype(np.float64)
         want = ref.float().cpu().numpy().astype(np.float64)
         assert_within_tolerance(got, want, cabs, name, f"noalloc call {call}")
-        assert torch.equal(out, ref)
+        assert torch.equal(out, ref)   # the same kernel and arithmetic: identical results
 
 
 def test_noalloc_rejects_bad_arguments(F):
