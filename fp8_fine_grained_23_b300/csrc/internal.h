@@ -17,7 +17,7 @@ constexpr int GEMM_BM = 128;
 constexpr int GEMM_BN = 256;
 constexpr int GEMM_BK = 128;
 constexpr int GEMM_MAX_GROUPS = 1024;
-constexpr int GEMM_DENSE_CLUSTER = 2;   // dense GEMM: CTA pairs sharing (multicasting) W tiles
+constexpr int GEMM_DENSE_CLUSTER = 2;   // dense GEMM: CTA pairs; each CTA loads half of the W tile
 
 // Device error word codes (the first error of a launch wins).
 enum DeviceError : int {

@@ -96,19 +96,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
-// Same load, written to the same shared-memory offset of every CTA in `cta_mask` (cluster
-// multicast); each destination CTA's mbarrier at offset `bar` receives the byte count.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* map,
-                                                      uint32_t bar, int32_t x, int32_t y,
-                                                      uint16_t cta_mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(map), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
-        : "memory");
-}
-
 // ------------------------------------------------------------------------------------
 // Thread-block clusters
 // ------------------------------------------------------------------------------------
@@ -292,16 +279,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar)
 {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-        : "memory");
-}
-
-// Arrives once on the mbarrier at offset `bar` of every CTA in `cta_mask` when the tcgen05.mma
-// issued so far by this thread have completed.
-__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t cta_mask)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(bar), "h"(cta_mask)
         : "memory");
 }
 
