@@ -50,3 +50,22 @@ def test_reduce_max_over_two_gloo_ranks():
     (r0, got0, _), (r1, got1, ref1) = res
     assert got0 == got1 == [2.0, 10.0, 0.5]
     assert ref1 is None              # the reference arm runs on rank 0 only
+
+
+@pytest.mark.timeout(300)
+def test_gpus_flag_starts_the_ranks_itself():
+    """`bench.py --gpus 2` with no external launcher starts two ranks (gloo on CPU for the
+    reference arm); rank 0 alone prints one JSON line that reports both ranks."""
+    import json
+    import subprocess
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2",
+                          "--impl", "reference", "--steps", "1", "--warmup", "3",
+                          "--ref-budget-s", "1"], env=env, capture_output=True, text=True,
+                         timeout=280)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [ln for ln in res.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, res.stdout
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2

@@ -65,3 +65,23 @@ def test_clock_sampler_summary():
     import json
     assert "NaN" not in json.dumps(out)
     assert _sampler_from_rows(bench, [], memory=True) is None
+
+
+def test_fp8_peak_follows_sampled_clocks():
+    """The step's GEMM is compared with the burst peak unless the timed region's clocks show the
+    power-capped state the sustained figure was measured in."""
+    bench = _bench()
+    peaks = {"hbm_gbs": 6425.0, "bf16_tflops": 1808.6, "bf16_tflops_sustained": 1390.4,
+             "sustained_sm_mhz": 1192.0}
+    full = {"sm_mhz": 2032.0, "sm_max_mhz": 2032.0, "reasons": []}
+    peak, burst, note = bench.choose_fp8_peak(peaks, full)
+    assert peak == burst == 2 * 1808.6 and "burst" in note
+    assert bench.choose_fp8_peak(peaks, None)[0] == 2 * 1808.6
+    # power cap at a clock well above the one the sustained figure was taken at: still burst
+    warm = {"sm_mhz": 1560.0, "sm_max_mhz": 2032.0, "reasons": ["sw_power_cap"]}
+    assert bench.choose_fp8_peak(peaks, warm)[0] == 2 * 1808.6
+    capped = {"sm_mhz": 1200.0, "sm_max_mhz": 2032.0, "reasons": ["sw_power_cap"]}
+    peak, burst, note = bench.choose_fp8_peak(peaks, capped)
+    assert peak == 2 * 1390.4 and burst == 2 * 1808.6 and "sustained" in note
+    # no recorded clock for the sustained figure: burst
+    assert bench.choose_fp8_peak(dict(peaks, sustained_sm_mhz=None), capped)[0] == 2 * 1808.6
