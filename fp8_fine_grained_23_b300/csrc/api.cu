@@ -155,19 +155,17 @@ int check_transpose_quant_args(const void* in, int64_t rows, int64_t K, int64_t 
     return FP8BS_OK;
 }
 
-// Dense GEMM launch shared by fp8_blockscaled_gemm (block-scaled W) and
-// fp8_blockscaled_gemm_1d1d (per-row B scales): the same tiles, maps and persistent grid.
-int dense_gemm(GemmKind kind, const uint8_t* a_q, const float* a_s, const uint8_t* w_q,
-               const float* w_s, int64_t M, int64_t N, int64_t K, void* c, int64_t ldc,
-               int out_dtype, fp8bs_stream_t stream, float* c_s = nullptr)
+// Dense GEMM launch shared by fp8_blockscaled_gemm (block-scaled W), fp8_blockscaled_gemm_1d1d
+// (per-row B scales), fp8_blockscaled_gemm_quant and the allocation-free entry point: the same
+// dispatch (few-row kernel for M <= GEMM_SMALL_MAX_M, else the CTA-pair kernel), tiles, maps and
+// persistent grid. The arguments have been checked and M > 0; `err` is the device error word the
+// kernels record a timeout in.
+int dense_gemm_launch(DeviceInfo* d, int* err, GemmKind kind, const uint8_t* a_q,
+                      const float* a_s, const uint8_t* w_q, const float* w_s, int64_t M, int64_t N,
+                      int64_t K, void* c, int64_t ldc, int out_dtype, fp8bs_stream_t stream,
+                      float* c_s)
 {
-    int st = kind == GemmKind::DENSE_QUANT ? FP8BS_OK
-                                           : check_gemm_args(a_q, a_s, w_q, w_s, M, N, K, c, ldc,
-                                                             out_dtype);
-    if (st != FP8BS_OK || M == 0) return st;
-    DeviceInfo* d = nullptr;
-    if ((st = current_device(&d)) != FP8BS_OK) return st;
-    if ((st = ensure_error_word(d)) != FP8BS_OK) return st;
+    int st = FP8BS_OK;
     if ((st = ensure_encoder()) != FP8BS_OK) return st;
 
     if (kind == GemmKind::DENSE && M <= GEMM_SMALL_MAX_M) {
@@ -192,7 +190,7 @@ int dense_gemm(GemmKind kind, const uint8_t* a_q, const float* a_s, const uint8_
         while (sa.split < 8 && items * sa.split * 2 <= d->num_sms && sa.KB >= 4 * sa.split)
             sa.split *= 2;
         if (items * sa.split > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
-        sa.err = d->err;
+        sa.err = err;
         sa.budget = wait_budget();
         return cuda_status(launch_gemm_small(mw, ma, sa, bnt, out_dtype == FP8BS_OUT_F32,
                                              reinterpret_cast<cudaStream_t>(stream)));
@@ -217,14 +215,30 @@ int dense_gemm(GemmKind kind, const uint8_t* a_q, const float* a_s, const uint8_
     const int64_t items = static_cast<int64_t>((args.MT + cluster - 1) / cluster) * args.NT;
     if (items > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
     args.num_tiles = static_cast<int>(items);
+    args.band = gemm_band((args.MT + cluster - 1) / cluster, args.NT, K, d->num_sms / cluster);
     args.offsets = nullptr;
     args.h_s = c_s;
     args.G = 1;
-    args.err = d->err;
+    args.err = err;
     args.budget = wait_budget();
     args.fault_skip_release = -1;
     return cuda_status(launch_gemm(ma, mb, args, kind, out_dtype == FP8BS_OUT_F32, d->num_sms,
                                    reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int dense_gemm(GemmKind kind, const uint8_t* a_q, const float* a_s, const uint8_t* w_q,
+               const float* w_s, int64_t M, int64_t N, int64_t K, void* c, int64_t ldc,
+               int out_dtype, fp8bs_stream_t stream, float* c_s = nullptr)
+{
+    int st = kind == GemmKind::DENSE_QUANT ? FP8BS_OK
+                                           : check_gemm_args(a_q, a_s, w_q, w_s, M, N, K, c, ldc,
+                                                             out_dtype);
+    if (st != FP8BS_OK || M == 0) return st;
+    DeviceInfo* d = nullptr;
+    if ((st = current_device(&d)) != FP8BS_OK) return st;
+    if ((st = ensure_error_word(d)) != FP8BS_OK) return st;
+    return dense_gemm_launch(d, d->err, kind, a_q, a_s, w_q, w_s, M, N, K, c, ldc, out_dtype,
+                             stream, c_s);
 }
 
 // Grouped launch shared by the plain grouped GEMM and the SwiGLU + re-quantizing one; the
@@ -259,6 +273,7 @@ int grouped_gemm(GemmKind kind, const uint8_t* a_q, const float* a_s, const uint
     args.NT = static_cast<int>((N + GEMM_BN - 1) / GEMM_BN);
     args.MT = 0;
     args.num_tiles = 0;
+    args.band = 1;
     args.offsets = group_offsets;
     args.h_s = h_s;
     args.G = static_cast<int>(G);
@@ -282,9 +297,7 @@ int quant_act(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q, int6
     if (st != FP8BS_OK || M == 0) return st;
     DeviceInfo* d = nullptr;
     if ((st = current_device(&d)) != FP8BS_OK) return st;
-    if ((st = ensure_error_word(d)) != FP8BS_OK) return st;
-    return cuda_status(launch_quant_act(x, M, K, ldx, q, ldq, scales, d->num_sms, d->err,
-                                        wait_budget(), ue8m0,
+    return cuda_status(launch_quant_act(x, M, K, ldx, q, ldq, scales, ue8m0,
                                         reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -490,13 +503,16 @@ int fp8bs_last_error(fp8bs_stream_t stream)
         cudaGetLastError();
         return FP8BS_ERR_CUDA;
     }
-    if (!d->err) return FP8BS_OK;
+    // The allocation-free GEMM records its timeouts in its own word inside the library image.
+    bool noalloc_timeout = false;
+    if ((st = noalloc_take_error(&noalloc_timeout)) != FP8BS_OK) return st;
+    if (!d->err) return noalloc_timeout ? FP8BS_ERR_TIMEOUT : FP8BS_OK;
     int h = 0;
     if (cudaMemcpy(&h, d->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) {
         cudaGetLastError();
         return FP8BS_ERR_CUDA;
     }
-    if (h == DEV_OK) return FP8BS_OK;
+    if (h == DEV_OK) return noalloc_timeout ? FP8BS_ERR_TIMEOUT : FP8BS_OK;
     if (cudaMemset(d->err, 0, sizeof(int)) != cudaSuccess) {
         cudaGetLastError();
         return FP8BS_ERR_CUDA;

@@ -50,12 +50,12 @@ struct GemmArgs {
     long long budget;         // spin-wait budget in SM clock cycles
     int fault_skip_release;   // test hook: accumulation index at which one epilogue warp skips
                               // its TMEM release (-1: never); set by fp8bs_debug_skip_release
+    int band;                 // dense: m-groups per band of the tile order (see gemm_band)
 };
 
 // ue8m0: power-of-two tile scales (tile_scale_ue8m0) instead of amax / 448
 cudaError_t launch_quant_act(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
-                             int64_t ldq, float* scales, int num_sms, int* err, long long budget,
-                             bool ue8m0, cudaStream_t stream);
+                             int64_t ldq, float* scales, bool ue8m0, cudaStream_t stream);
 cudaError_t launch_quant_weight(const void* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
                                 int64_t ldq, float* scales, bool ue8m0, cudaStream_t stream);
 cudaError_t launch_moe_permute(const uint8_t* q, int64_t ldq, const float* s, int64_t T,
@@ -102,6 +102,9 @@ enum class GemmKind { DENSE, GROUPED, ROW_SCALED, GROUPED_SWIGLU, DENSE_QUANT };
 cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args,
                         GemmKind kind, bool out_f32, int max_ctas, cudaStream_t stream);
 int gemm_cluster_size(bool grouped);
+// Dense tile order: m-groups (of cluster-size m-tiles) per band for a problem of `mgroups` x `NT`
+// items with K bytes of codes per row, on `clusters` concurrent clusters.
+int gemm_band(int mgroups, int NT, int64_t K, int clusters);
 size_t gemm_smem_bytes(GemmKind kind, int G);
 
 // ------------------------------------------------------------------------------------
@@ -131,6 +134,14 @@ int check_quant_args(const void* in, int64_t rows, int64_t K, int64_t ld_in, con
                      int64_t ldq, const void* scales);
 int check_gemm_args(const void* a_q, const void* a_s, const void* w_q, const void* w_s,
                     int64_t rows, int64_t N, int64_t K, const void* c, int64_t ldc, int out_dtype);
+// The dense GEMM dispatch after the argument checks (M > 0), with the error word `err`.
+int dense_gemm_launch(DeviceInfo* d, int* err, GemmKind kind, const uint8_t* a_q,
+                      const float* a_s, const uint8_t* w_q, const float* w_s, int64_t M, int64_t N,
+                      int64_t K, void* c, int64_t ldc, int out_dtype, fp8bs_stream_t stream,
+                      float* c_s);
+// Reads and clears the allocation-free entry point's error word on the current device (if that
+// entry point has run there); *timeout is set when a launch recorded a timeout (noalloc.cu).
+int noalloc_take_error(bool* timeout);
 
 }  // namespace host
 

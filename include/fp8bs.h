@@ -291,19 +291,22 @@ int fp8_blockscaled_gemm_quant(const uint8_t *a_q, const float *a_s,
  * fp8_blockscaled_gemm allocates a 4-byte error word with cudaMalloc on its first call on a
  * device; this variant never calls cudaMalloc, cudaFree or any allocating routine.
  *
- * Instead its kernel keeps that scratch word in a fixed 256-byte array inside the library image
+ * Instead its kernels keep that scratch word in a fixed 256-byte array inside the library image
  * (a static __device__ array: every GPU that loads the library holds it until the process exits).
  * A call needs one 4-byte word of it for any problem size; a call that would need more than the
  * array holds is rejected with FP8BS_ERR_INVALID_ARG before anything is launched.
  *
  * The first call on a device looks up the array's device address (once per device, with that
- * device current); make that first call before any stream capture begins. Every call clears the
- * word on `stream` before its launch, and every call shares the same array: calls that can
- * overlap on the GPU (different streams without ordering between them) race on it, so order them.
- * A pipeline timeout of this variant is recorded in that shared word, which fp8bs_last_error()
- * does not read; callers that need that status use fp8_blockscaled_gemm.
+ * device current); make that first call before any stream capture begins. Every call shares the
+ * same array and it keeps what the last call left there: the word is zero when the library is
+ * loaded, a kernel only ever moves it from zero to a timeout code, and fp8bs_last_error() reads
+ * it (beside the regular error word) and sets it back to zero, so a timeout stays recorded until
+ * it is read. Calls that can overlap on the GPU (different streams without ordering between them)
+ * race on that word, and a recorded timeout cannot then be attributed to one of them: order them.
  *
- * Arguments, layouts, requirements and results are exactly those of fp8_blockscaled_gemm.
+ * Dispatch, arguments, layouts, requirements and results are exactly those of
+ * fp8_blockscaled_gemm (the few-row kernel for M <= 64, the CTA-pair kernel above), so the two
+ * calls return identical outputs.
  */
 int fp8_blockscaled_gemm_noalloc(const uint8_t *a_q, const float *a_s,
                                  const uint8_t *w_q, const float *w_s,
@@ -325,9 +328,11 @@ int fp8bs_debug_skip_release(int at);
 const char *fp8bs_status_string(int status);
 
 /*
- * Synchronizes `stream`, then reads and clears the current device's error word, which the
- * GEMM kernels set when a pipeline wait runs past its budget (they then stop, drain their
- * in-flight copies and return). Returns FP8BS_OK, FP8BS_ERR_TIMEOUT or FP8BS_ERR_CUDA.
+ * Synchronizes `stream`, then reads and clears the current device's error words: the one the
+ * GEMM and quantizer kernels set when a pipeline wait runs past its budget (they then stop, drain
+ * their in-flight copies and return), and the one inside the library image that
+ * fp8_blockscaled_gemm_noalloc's kernels use. Allocates nothing. Returns FP8BS_OK,
+ * FP8BS_ERR_TIMEOUT (either word recorded a timeout) or FP8BS_ERR_CUDA.
  */
 int fp8bs_last_error(fp8bs_stream_t stream);
 
