@@ -71,61 +71,22 @@ __device__ __forceinline__ void st_v2(void* p, const uint2& v)
 }
 
 // ------------------------------------------------------------------------------------
-// 1x128 activation tiles: persistent CTAs, TMA-staged, one tile per lane.
+// 1x128 activation tiles: one warp per run of QA_TILES consecutive tiles of one row.
 //
-// The rows are cut into segments of up to 32 tiles (8 KB of BF16) of one row; each CTA owns a
-// contiguous, balanced range of segments. Segment i of a CTA belongs to consumer warp i % QA_CONSUMERS,
-// which owns QA_SLOTS_PER_WARP shared-memory slots and consumes them strictly in order (so every
-// slot's mbarriers see one producer and one consumer, phase after phase). A producer thread
-// streams the segments, in order, into the slots with bulk copies (QA_SLOTS x 8 KB in flight
-// per CTA). A consumer warp takes a whole segment: lane l loads tile l (16 x 16 B, rotated so that the reads are free of
-// bank conflicts), reduces its amax with packed 16-bit integer maxima on |bits| (exact for
-// finite BF16), computes its scale and reciprocal (one division pass covers 32 tiles), and
-// encodes its 128 values. The codes are written back into the slot and then copied out with
-// coalesced 16-byte stores (512 contiguous bytes per warp instruction).
+// Half-warp h holds the tiles 2i + h (i < QA_TILES / 2) of the run; lane l16 of the half holds
+// eight values (16 bytes) of each, so every load instruction of the warp reads 512 contiguous
+// bytes of the row, and all of a warp's loads are issued before any is used (QA_TILES * 256
+// bytes in flight per warp, six 8-warp CTAs per SM). A tile's amax is the packed 16-bit
+// maximum of |bits| over the lane's eight values (exact for finite BF16), reduced over the 16
+// lanes of its half by four xor shuffles, two tiles per 32-bit word. Lane l16 < QA_TILES / 2 then
+// forms the scale of its half's tile 2 l16 + h (the two IEEE divisions run once per tile and are
+// stored by that lane), and every lane receives r and the tile's mode by shuffles to encode its
+// values; each store instruction writes 256 contiguous code bytes. No shared memory, no waits.
 // ------------------------------------------------------------------------------------
-constexpr int SEG_TILES = 32;
-constexpr int SEG_BYTES = SEG_TILES * 256;
-constexpr int QA_CONSUMERS = 6;
-constexpr int QA_SLOTS_PER_WARP = 2;
-constexpr int QA_SLOTS = QA_CONSUMERS * QA_SLOTS_PER_WARP;
-constexpr int QA_THREADS = (QA_CONSUMERS + 1) * 32;
-constexpr int QA_CTAS_PER_SM = 2;
-constexpr int QA_SMEM = QA_SLOTS * SEG_BYTES + 2 * QA_SLOTS * 8 + 16 + 128;
-
-struct QuantActArgs {
-    const uint16_t* x;
-    int64_t M;
-    int KB;
-    int64_t ldx;
-    uint8_t* q;
-    int64_t ldq;
-    float* scales;
-    int* err;
-    long long budget;
-};
-
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
-{
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_shared_v2(uint32_t addr, const uint2& v)
-{
-    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(v.x), "r"(v.y) : "memory");
-}
-
-__device__ __forceinline__ void st_global_v4(void* p, const uint4& v)
-{
-    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
-                 "r"(v.w)
-                 : "memory");
-}
+constexpr int QA_TILES = 8;            // tiles per warp
+constexpr int QA_WARPS = 8;            // warps per CTA
+constexpr int QA_THREADS = QA_WARPS * 32;
+constexpr int QA_CTAS_PER_SM = 6;      // 40 registers: 48 warps, 96 KB of loads in flight per SM
 
 __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b)
 {
@@ -134,145 +95,65 @@ __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b)
     return r;
 }
 
-// max |x| over eight BF16 values held as four 32-bit words: for finite BF16 the magnitude order
-// is the unsigned order of the bits with the sign cleared.
-__device__ __forceinline__ uint32_t absmax_bits_u16x2(const uint4& v, uint32_t m)
+// max |x| of eight BF16 values held as four 32-bit words, as BF16 bits: for finite BF16 the
+// magnitude order is the unsigned order of the bits with the sign cleared.
+__device__ __forceinline__ uint32_t absmax_bits8(const uint4& v)
 {
-    m = max_u16x2(m, v.x & 0x7FFF7FFFu);
-    m = max_u16x2(m, v.y & 0x7FFF7FFFu);
+    uint32_t m = max_u16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu);
     m = max_u16x2(m, v.z & 0x7FFF7FFFu);
-    return max_u16x2(m, v.w & 0x7FFF7FFFu);
-}
-
-// Slot and barrier phase of a CTA's i-th segment: consumer warp w = i % QA_CONSUMERS handles
-// its k-th segment (k = i / QA_CONSUMERS) in its own slot w * QA_SLOTS_PER_WARP +
-// k % QA_SLOTS_PER_WARP, which it has used k / QA_SLOTS_PER_WARP times before.
-__device__ __forceinline__ uint32_t qa_slot(int64_t i)
-{
-    const int64_t w = i % QA_CONSUMERS, k = i / QA_CONSUMERS;
-    return static_cast<uint32_t>(w * QA_SLOTS_PER_WARP + k % QA_SLOTS_PER_WARP);
-}
-
-__device__ __forceinline__ uint32_t qa_phase(int64_t i)
-{
-    return static_cast<uint32_t>((i / QA_CONSUMERS) / QA_SLOTS_PER_WARP) & 1u;
+    m = max_u16x2(m, v.w & 0x7FFF7FFFu);
+    return max(m & 0xFFFFu, m >> 16);
 }
 
 template <bool UE8M0>
 __global__ void __launch_bounds__(QA_THREADS, QA_CTAS_PER_SM)
-quant_act_1x128_kernel(const QuantActArgs p)
+quant_act_1x128_kernel(const uint16_t* __restrict__ x, int64_t M, int KB, int64_t ldx,
+                       uint8_t* __restrict__ q, int64_t ldq, float* __restrict__ scales)
 {
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 127u) & ~127u;
-    const uint32_t bar_full = base + QA_SLOTS * SEG_BYTES;
-    const uint32_t bar_empty = bar_full + 8 * QA_SLOTS;
-    const uint32_t abort_addr = bar_empty + 8 * QA_SLOTS;   // shared word: a role gave up
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int KB = p.KB;
-    const int segs_per_row = (KB + SEG_TILES - 1) / SEG_TILES;
-    const int64_t total = p.M * segs_per_row;
-    const int64_t s_begin = total * blockIdx.x / gridDim.x;
-    const int64_t nseg = total * (blockIdx.x + 1) / gridDim.x - s_begin;
-
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < QA_SLOTS; i++) {
-            mbar_init(bar_full + 8 * i, 1);
-            mbar_init(bar_empty + 8 * i, 1);
-        }
-        st_shared_volatile_u32(abort_addr, 0u);
-        fence_mbar_init();
+    constexpr int H = QA_TILES / 2;   // tiles per half-warp
+    const int lane = threadIdx.x & 31, half = lane >> 4, l16 = lane & 15;
+    const int runs = (KB + QA_TILES - 1) / QA_TILES;
+    const int64_t wid = static_cast<int64_t>(blockIdx.x) * QA_WARPS + (threadIdx.x >> 5);
+    if (wid >= M * runs) return;      // whole warps only
+    const int64_t row = wid / runs;
+    const int tile0 = static_cast<int>(wid % runs) * QA_TILES;
+    const int nt = min(QA_TILES, KB - tile0);
+    const uint16_t* src = x + row * ldx + static_cast<int64_t>(tile0) * 128 + l16 * 8;
+    uint4 v[H];
+#pragma unroll
+    for (int i = 0; i < H; i++) {
+        const int t = 2 * i + half;
+        v[i] = t < nt ? ld_stream_v4(src + t * 128) : make_uint4(0u, 0u, 0u, 0u);
     }
-    __syncthreads();
-
-    if (warp == QA_CONSUMERS) {
-        // ------------------------------------------------------------ producer
-        if (lane == 0) {
-            int64_t i = 0;
-            bool ok = true;
-            for (; i < nseg; i++) {
-                const uint32_t slot = qa_slot(i);
-                const uint32_t ph = qa_phase(i);
-                if (!mbar_wait(bar_empty + 8 * slot, ph ^ 1u, abort_addr, p.budget)) {
-                    st_shared_volatile_u32(abort_addr, 1u);
-                    atomicCAS(p.err, 0, DEV_TIMEOUT_PRODUCER);
-                    ok = false;
-                    break;
-                }
-                const int64_t seg = s_begin + i;
-                const int64_t row = seg / segs_per_row;
-                const int tile0 = static_cast<int>(seg % segs_per_row) * SEG_TILES;
-                const int nt = min(SEG_TILES, KB - tile0);
-                const uint32_t bytes = static_cast<uint32_t>(nt) * 256u;
-                mbar_arrive_expect_tx(bar_full + 8 * slot, bytes);
-                bulk_load(base + slot * SEG_BYTES, p.x + row * p.ldx + static_cast<int64_t>(tile0) * 128,
-                          bytes, bar_full + 8 * slot);
-            }
-            if (!ok || ld_shared_volatile_u32(abort_addr) != 0) {
-                // after an abort, wait for the copies already issued before the CTA exits
-                for (int64_t j = (i > QA_SLOTS ? i - QA_SLOTS : 0); j < i; j++)
-                    if (!mbar_wait(bar_full + 8 * qa_slot(j), qa_phase(j), 0u, p.budget))
-                        atomicCAS(p.err, 0, DEV_TIMEOUT_DRAIN);
-            }
-        }
-    } else {
-        // ------------------------------------------------------------ consumers
-        for (int64_t i = warp; i < nseg; i += QA_CONSUMERS) {
-            const uint32_t slot = qa_slot(i);
-            const uint32_t ph = qa_phase(i);
-            const bool got = mbar_wait(bar_full + 8 * slot, ph, abort_addr, p.budget);
-            if (!__all_sync(0xffffffffu, got)) {
-                if (lane == 0) {
-                    st_shared_volatile_u32(abort_addr, 1u);
-                    atomicCAS(p.err, 0, DEV_TIMEOUT_EPILOGUE);
-                }
-                break;
-            }
-            const int64_t seg = s_begin + i;
-            const int64_t row = seg / segs_per_row;
-            const int tile0 = static_cast<int>(seg % segs_per_row) * SEG_TILES;
-            const int nt = min(SEG_TILES, KB - tile0);
-            const bool active = lane < nt;
-            const uint32_t slot_base = base + slot * SEG_BYTES;
-            const uint32_t my_tile = slot_base + lane * 256;
-
-            uint4 v[16];
+    // P[k]: this half's tiles 4k + h (low 16 bits) and 4k + 2 + h (high 16 bits)
+    uint32_t P[H / 2];
 #pragma unroll
-            for (int j = 0; j < 16; j++) {
-                const int c = (j + lane) & 15;
-                v[j] = active ? ld_shared_v4(my_tile + c * 16) : make_uint4(0u, 0u, 0u, 0u);
-            }
-            uint32_t m2 = 0;
+    for (int k = 0; k < H / 2; k++) P[k] = absmax_bits8(v[2 * k]) | (absmax_bits8(v[2 * k + 1]) << 16);
 #pragma unroll
-            for (int j = 0; j < 16; j++) m2 = absmax_bits_u16x2(v[j], m2);
-            const uint32_t mbits = max(m2 & 0xFFFFu, m2 >> 16);
-            const TileScale ts = tile_scale_of<UE8M0>(__uint_as_float(mbits << 16));
-            __syncwarp();   // every lane holds its tile before the codes overwrite the slot
-
+    for (int o = 8; o > 0; o >>= 1) {
 #pragma unroll
-            for (int j = 0; j < 16; j++) {
-                const int c = (j + lane) & 15;
-                float f[8];
-                unpack_bf16x8(v[j], f);
-                const uint2 codes = encode8(f, ts);
-                if (active) st_shared_v2(slot_base + lane * 128 + c * 8, codes);
-            }
-            __syncwarp();
-
-            const int code_bytes = nt * 128;
-            uint8_t* qrow = p.q + row * p.ldq + static_cast<int64_t>(tile0) * 128;
+        for (int k = 0; k < H / 2; k++) P[k] = max_u16x2(P[k], __shfl_xor_sync(0xffffffffu, P[k], o));
+    }
+    uint32_t mine = 0;   // amax bits of tile 2 * l16 + half (lanes l16 < H)
 #pragma unroll
-            for (int j = 0; j < SEG_TILES * 128 / 512; j++) {
-                const int off = j * 512 + lane * 16;
-                if (off < code_bytes) st_global_v4(qrow + off, ld_shared_v4(slot_base + off));
-            }
-            if (active) p.scales[static_cast<int64_t>(tile0 + lane) * p.M + row] = ts.s;
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty + 8 * slot);
-        }
+    for (int k = 0; k < H / 2; k++)
+        if ((l16 >> 1) == k) mine = (l16 & 1) ? (P[k] >> 16) : (P[k] & 0xFFFFu);
+    const TileScale ts = tile_scale_of<UE8M0>(__uint_as_float(mine << 16));
+    const int my_tile = 2 * l16 + half;
+    if (l16 < H && my_tile < nt) scales[static_cast<int64_t>(tile0 + my_tile) * M + row] = ts.s;
+    const uint32_t mode = (ts.tiny ? 1u : 0u) | (ts.zero ? 2u : 0u);
+    uint8_t* dst = q + row * ldq + static_cast<int64_t>(tile0) * 128 + l16 * 8;
+#pragma unroll
+    for (int i = 0; i < H; i++) {
+        TileScale ti;
+        ti.r = __shfl_sync(0xffffffffu, ts.r, (half << 4) + i);
+        const uint32_t md = __shfl_sync(0xffffffffu, mode, (half << 4) + i);
+        ti.tiny = (md & 1u) != 0;
+        ti.zero = (md & 2u) != 0;
+        const int t = 2 * i + half;
+        float f[8];
+        unpack_bf16x8(v[i], f);
+        if (t < nt) st_v2(dst + t * 128, encode8(f, ti));
     }
 }
 
@@ -329,6 +210,28 @@ quant_weight_128x128_kernel(const uint16_t* __restrict__ w, int64_t N, int KB, i
         }
     }
     if (threadIdx.x == 0) scales[nb * KB + kb] = ts.s;
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_shared_v2(uint32_t addr, const uint2& v)
+{
+    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(v.x), "r"(v.y) : "memory");
+}
+
+__device__ __forceinline__ void st_global_v4(void* p, const uint4& v)
+{
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
 }
 
 // ------------------------------------------------------------------------------------
@@ -454,26 +357,15 @@ quant_transpose_kernel(const uint16_t* __restrict__ x, int64_t ldx, uint8_t* __r
 }  // namespace
 
 cudaError_t launch_quant_act(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
-                             int64_t ldq, float* scales, int num_sms, int* err, long long budget,
-                             bool ue8m0, cudaStream_t stream)
+                             int64_t ldq, float* scales, bool ue8m0, cudaStream_t stream)
 {
-    QuantActArgs a;
-    a.x = static_cast<const uint16_t*>(x);
-    a.M = M;
-    a.KB = static_cast<int>(K / 128);
-    a.ldx = ldx;
-    a.q = q;
-    a.ldq = ldq;
-    a.scales = scales;
-    a.err = err;
-    a.budget = budget;
-    const int64_t segs = M * ((a.KB + SEG_TILES - 1) / SEG_TILES);
-    const int64_t cap = static_cast<int64_t>(num_sms) * QA_CTAS_PER_SM;
-    const int grid = static_cast<int>(segs < cap ? segs : cap);
+    const int KB = static_cast<int>(K / 128);
+    const int64_t warps = M * ((KB + QA_TILES - 1) / QA_TILES);
+    const int64_t grid = (warps + QA_WARPS - 1) / QA_WARPS;
+    if (grid > INT32_MAX) return cudaErrorInvalidConfiguration;
     auto kern = ue8m0 ? quant_act_1x128_kernel<true> : quant_act_1x128_kernel<false>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, QA_SMEM);
-    if (e != cudaSuccess) return e;
-    kern<<<grid, QA_THREADS, QA_SMEM, stream>>>(a);
+    kern<<<static_cast<unsigned>(grid), QA_THREADS, 0, stream>>>(static_cast<const uint16_t*>(x), M,
+                                                                 KB, ldx, q, ldq, scales);
     return cudaGetLastError();
 }
 

@@ -48,7 +48,8 @@ def test_tiny_workload(F):
     check_weight(F, w)
 
 
-@pytest.mark.parametrize("M,K", [(1, 128), (3, 256), (5, 384), (129, 640), (257, 1536)])
+@pytest.mark.parametrize("M,K", [(1, 128), (3, 256), (5, 384), (129, 640), (257, 1536), (33, 1152),
+                                 (2, 1024)])
 def test_act_ragged_shapes(F, M, K):
     g = W.generator(100 + M, "cpu")
     check_act(F, W.activations(M, K, g, "cpu", zero_tile_p=0.05))
