@@ -18,6 +18,10 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_PATH = os.path.join(PKG, "libfp8bs.so")
+# Debug build with a serialised pipeline (GEMMs: one operand stage, one scale slot, one TMEM
+# accumulator): every role waits for the previous one at every step, so a missing or misplaced
+# barrier shows up as a different result or a timeout. Tests only.
+SERIAL_LIB_PATH = os.path.join(PKG, "libfp8bs_serial.so")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 
@@ -30,10 +34,10 @@ def sources() -> list[str]:
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def _stale(path: str = LIB_PATH) -> bool:
+    if not os.path.exists(path):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     deps = sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(
         os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(INCLUDE, "*.h"))
     return any(os.path.getmtime(d) > t for d in deps)
@@ -66,13 +70,15 @@ def resource_report(ptxas_log: str) -> dict[str, dict[str, int]]:
     return out
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    if not force and not _stale():
-        return LIB_PATH
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+def build(force: bool = False, verbose_ptxas: bool = False, serial: bool = False) -> str:
+    path = SERIAL_LIB_PATH if serial else LIB_PATH
+    if not force and not _stale(path):
+        return path
+    tmp = path + f".tmp{os.getpid()}"
     cmd = [_nvcc(), ARCH, "-O3", "-lineinfo", "-std=c++17", "-prec-div=true", "-prec-sqrt=true",
            "-ftz=false", "-Xptxas=-v", "-Xcompiler", "-fPIC,-O2,-Wall", "-shared", "-cudart",
-           "static", "-I", INCLUDE, "-I", CSRC, *sources(), "-o", tmp]
+           "static", *(["-DFP8BS_SERIAL_PIPELINE"] if serial else []), "-I", INCLUDE, "-I", CSRC,
+           *sources(), "-o", tmp]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         sys.stderr.write(res.stdout + res.stderr)
@@ -86,9 +92,10 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
     if verbose_ptxas:
         for name, r in report.items():
             print(f"{name}: {r}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, path)
+    return path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose_ptxas="-v" in sys.argv,
+                serial="--serial" in sys.argv))

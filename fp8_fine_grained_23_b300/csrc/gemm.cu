@@ -81,13 +81,22 @@ constexpr int REGS_CONTROL = 72;           // warpgroup 0 after setmaxnreg.dec
 constexpr int REGS_EPILOGUE = 216;         // warpgroups 1 and 2 after setmaxnreg.inc
 static_assert(128 * REGS_CONTROL + 256 * REGS_EPILOGUE == THREADS * 168,
               "register split must equal the launch allocation of 168 per thread");
-constexpr int TMEM_COLS = 2 * BN;          // two FP32 accumulators of 128 lanes x BN columns
+// FP8BS_SERIAL_PIPELINE (a debug build, see build.py --serial): one operand stage, one scale
+// slot and one TMEM accumulator, so that every role waits for the previous one at every K block;
+// results must not change.
+#ifdef FP8BS_SERIAL_PIPELINE
+constexpr bool SERIAL = true;
+#else
+constexpr bool SERIAL = false;
+#endif
+constexpr int TMEM_BUFS = SERIAL ? 1 : 2;  // FP32 accumulators of 128 lanes x BN columns
+constexpr int TMEM_COLS = TMEM_BUFS * BN;
 
 constexpr int A_BYTES = BM * BK;           // E4M3: one byte per element
 constexpr int B_BYTES = BN * BK;           // the whole W tile
 constexpr int STG_WARP_BYTES = 32 * 64;    // output staging per epilogue warp: 32 rows x 64 B
 constexpr int STG_BYTES = NUM_EPI_WARPS * STG_WARP_BYTES;
-constexpr int SCALE_SLOTS = 8;             // scale ring: one slot per K block in flight
+constexpr int SCALE_SLOTS = SERIAL ? 1 : 8;   // scale ring: one slot per K block in flight
 constexpr int SCALE_SLOT_BYTES_BLOCK = 528;   // 128 activation scales + 2 weight-block scales
 constexpr int SCALE_SLOT_BYTES_ROWS = 1536;   // 128 A-row scales + 256 B-row scales
 constexpr int ALIGN_PAD = 1024;            // 128-byte-swizzled tiles need 1024-byte alignment
@@ -102,7 +111,7 @@ struct Layout {
     static constexpr int CL = PAIR ? 2 : 1;              // CTAs per cluster
     static constexpr int B_PART = B_BYTES / CL;          // W rows held by this CTA
     static constexpr int STAGE = A_BYTES + B_PART;
-    static constexpr int STAGES = PAIR ? 6 : 4;
+    static constexpr int STAGES = SERIAL ? 1 : (PAIR ? 6 : 4);
     static constexpr int A_OFF = 0;
     static constexpr int B_OFF = STAGES * A_BYTES;
     static constexpr int STG_OFF = STAGES * STAGE;
@@ -132,9 +141,12 @@ __device__ __forceinline__ void raise_error(int* err, uint32_t abort_addr, int c
 }
 
 // Work item t of a CTA whose rank in its cluster is `crank`. Dense: t numbers groups of CL
-// adjacent m-tiles (one per CTA of the cluster) on one n-tile, m fastest; an m-tile past the last
-// row reads zeros and stores nothing. Grouped (CL == 1): t numbers (group, n-tile, m-tile) with
-// m fastest, so the m-tiles of one expert's W tile run side by side.
+// adjacent m-tiles (one per CTA of the cluster) on one n-tile. The m-groups are cut into bands of
+// p.band; the items run band by band, and within a band m fastest, then n, so that the
+// concurrent CTAs share a few A panels and a few W panels that stay in L2 (p.band = all m-groups
+// gives plain m-fastest order). An m-tile past the last row reads zeros and stores nothing.
+// Grouped (CL == 1): t numbers (group, n-tile, m-tile) with m fastest, so the m-tiles of one
+// expert's W tile run side by side.
 template <bool GROUPED, int CL>
 __device__ __forceinline__ TileInfo decode_tile(int t, const GemmArgs& p, const int* s_tstart,
                                                 const int* s_off, int crank)
@@ -142,8 +154,12 @@ __device__ __forceinline__ TileInfo decode_tile(int t, const GemmArgs& p, const 
     TileInfo ti;
     if constexpr (!GROUPED) {
         const int mgroups = (p.MT + CL - 1) / CL;
-        const int mt = (t % mgroups) * CL + crank;
-        const int nt = t / mgroups;
+        const int per_band = p.band * p.NT;
+        const int mb0 = (t / per_band) * p.band;             // first m-group of t's band
+        const int bw = min(p.band, mgroups - mb0);           // m-groups in that band
+        const int r = t - mb0 * p.NT;                        // item within the band
+        const int mt = (mb0 + r % bw) * CL + crank;
+        const int nt = r / bw;
         ti.row0 = static_cast<int64_t>(mt) * BM;
         ti.row_end = p.rows;
         ti.n0 = nt * BN;
@@ -412,8 +428,8 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                 bool ok = true, issued = false;
                 for (int t = cluster_id; ok && t < num_tiles; t += num_clusters) {
                     for (int kb = 0; kb < KB; kb++, it++, j++) {
-                        const uint32_t b = j & 1u;
-                        const uint32_t pb = (j >> 1) & 1u;
+                        const uint32_t b = j % TMEM_BUFS;
+                        const uint32_t pb = (j / TMEM_BUFS) & 1u;
                         const bool freed = mbar_wait(tempty0 + 8 * b, pb ^ 1u, abort_addr, budget);
                         if (!freed) {
                             raise_error(p.err, abort_addr, DEV_TIMEOUT_MMA_TMEM);
@@ -466,8 +482,8 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                 bool ok = true;
                 for (int t = cluster_id; ok && t < num_tiles; t += num_clusters) {
                     for (int kb = 0; kb < KB; kb++, j++) {
-                        const uint32_t b = j & 1u;
-                        if (!mbar_wait(tempty0 + 8 * b, (j >> 1) & 1u, abort_addr, budget)) {
+                        const uint32_t b = j % TMEM_BUFS;
+                        if (!mbar_wait(tempty0 + 8 * b, (j / TMEM_BUFS) & 1u, abort_addr, budget)) {
                             raise_error(p.err, abort_addr, DEV_TIMEOUT_MMA_TMEM);
                             ok = false;
                             break;
@@ -586,8 +602,8 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     if (lane == 0) mbar_arrive(sempty0 + 8 * slot);
                 }
 
-                const uint32_t b = j & 1u;
-                const uint32_t pb = (j >> 1) & 1u;
+                const uint32_t b = j % TMEM_BUFS;
+                const uint32_t pb = (j / TMEM_BUFS) & 1u;
                 const bool got = mbar_wait(tfull0 + 8 * b, pb, abort_addr, budget);
                 if (!__all_sync(0xffffffffu, got)) {
                     if (lane == 0) raise_error(p.err, abort_addr, DEV_TIMEOUT_EPILOGUE);
@@ -921,6 +937,26 @@ size_t gemm_smem_bytes(GemmKind kind, int G)
 }
 
 int gemm_cluster_size(bool grouped) { return grouped ? 1 : GEMM_DENSE_CLUSTER; }
+
+// Dense tile order. The concurrent clusters of one wave read, over the whole K loop, the A
+// panels (cluster rows x K bytes) of the m-groups they cover and the W panels (BN x K bytes) of
+// the n-tiles they cover; the next wave finds a panel in L2 only if the wave's panels fit there.
+// Plain m-fastest order keeps all m-groups in every wave, which is best while that fits (all of
+// A is read once). Otherwise bands of about sqrt(clusters) m-groups make a wave's panels as few
+// as possible: each band's A panels are read once, the W panels once per band.
+int gemm_band(int mgroups, int NT, int64_t K, int clusters)
+{
+    constexpr double L2_BUDGET = 48.0 * 1024 * 1024;   // of the 126 MB L2, for one wave's panels
+    const double a_panel = static_cast<double>(GEMM_DENSE_CLUSTER * GEMM_BM) * K;
+    const double b_panel = static_cast<double>(GEMM_BN) * K;
+    const int P = clusters > 0 ? clusters : 1;
+    const int mw = mgroups < P ? mgroups : P;
+    const int nw = (P + mgroups - 1) / mgroups;
+    if (mw * a_panel + (nw < NT ? nw : NT) * b_panel <= L2_BUDGET) return mgroups > 0 ? mgroups : 1;
+    int b = 1;
+    while ((b + 1) * (b + 1) * a_panel <= P * b_panel) b++;   // b ~ sqrt(P * b_panel / a_panel)
+    return b < mgroups ? b : mgroups;
+}
 
 cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args,
                         GemmKind kind, bool out_f32, int max_ctas, cudaStream_t stream)

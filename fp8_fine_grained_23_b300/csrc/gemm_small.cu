@@ -39,7 +39,12 @@ struct SmallLayout {
     static constexpr int B_BYTES = BNT * SM_BK;          // token tile (the MMA's B operand)
     static constexpr int STAGE = A_BYTES + B_BYTES;
     // as many stages as fit in ~192 KB: the weight stream needs the bytes in flight
+#ifdef FP8BS_SERIAL_PIPELINE
+    // debug build (build.py --serial): the fewest stages whose ring still holds the partial tile
+    static constexpr int STAGES = (SM_BM * BNT * 4 + STAGE - 1) / STAGE;
+#else
     static constexpr int STAGES = (192 * 1024) / STAGE > 10 ? 10 : (192 * 1024) / STAGE;
+#endif
     static constexpr int A_OFF = 0;
     static constexpr int B_OFF = STAGES * A_BYTES;
     static constexpr int RING = STAGES * STAGE;
