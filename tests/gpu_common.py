@@ -15,6 +15,66 @@ from tests.helpers import bits_of, gemm_tolerance
 THREADS = max(1, min(32, os.cpu_count() or 1))
 
 
+GUARD_BYTES = 4096   # canary band on each side of every output the binding allocates
+GUARD_FILL = 0xA5
+
+
+class _GuardTorch:
+    """Stands in for `torch` inside the binding during one call: its `empty` returns a view into
+    a buffer with GUARD_BYTES of canary bytes before and after it, and records the buffer."""
+
+    def __init__(self, real, records):
+        self._real = real
+        self._records = records
+
+    def __getattr__(self, name):
+        return getattr(self._real, name)
+
+    def empty(self, *size, dtype=None, device=None):
+        if len(size) == 1 and isinstance(size[0], (tuple, list, torch.Size)):
+            size = tuple(size[0])
+        dtype = dtype or torch.float32
+        elem = torch.empty((), dtype=dtype).element_size()
+        pad = GUARD_BYTES // elem
+        numel = int(np.prod(size)) if size else 1
+        buf = self._real.empty(numel + 2 * pad, dtype=dtype, device=device)
+        buf.view(torch.uint8).fill_(GUARD_FILL)
+        self._records.append((buf, pad * elem))
+        return buf[pad:pad + numel].view(size)
+
+
+class GuardedBinding:
+    """The binding with guard bands around every output it allocates: each fp8_* call runs with
+    its outputs inside canary bands, and after the call (synchronized) both bands must still
+    hold the canary bytes, so a kernel that writes past either end of an output fails the test
+    that called it. Other attributes pass through."""
+
+    def __init__(self, mod):
+        self._mod = mod
+
+    def __getattr__(self, name):
+        v = getattr(self._mod, name)
+        if name.startswith("fp8_") and callable(v):
+            def call(*args, **kw):
+                records = []
+                real = self._mod.torch
+                self._mod.torch = _GuardTorch(real, records)
+                try:
+                    out = v(*args, **kw)
+                finally:
+                    self._mod.torch = real
+                if records:
+                    if torch.cuda.is_available():
+                        torch.cuda.synchronize()
+                    for buf, pad in records:
+                        b = buf.view(torch.uint8)
+                        bad = int((b[:pad] != GUARD_FILL).sum() + (b[b.numel() - pad:] != GUARD_FILL).sum())
+                        assert bad == 0, f"{name}: {bad} guard-band bytes around an output were written"
+                return out
+            return call
+        return v
+
+
 @pytest.fixture(scope="session")
 def F():
     if not torch.cuda.is_available():
@@ -22,7 +82,7 @@ def F():
     from fp8_fine_grained_23_b300 import build
     build.build()
     from fp8_fine_grained_23_b300 import fp8bs
-    return fp8bs
+    return GuardedBinding(fp8bs)
 
 
 def oracle_quant_act(x_bits: np.ndarray):
