@@ -329,8 +329,8 @@ const char *fp8bs_status_string(int status);
 
 /*
  * Synchronizes `stream`, then reads and clears the current device's error words: the one the
- * GEMM and quantizer kernels set when a pipeline wait runs past its budget (they then stop, drain
- * their in-flight copies and return), and the one inside the library image that
+ * GEMM kernels set when a pipeline wait runs past its budget (they then stop, drain their
+ * in-flight copies and return), and the one inside the library image that
  * fp8_blockscaled_gemm_noalloc's kernels use. Allocates nothing. Returns FP8BS_OK,
  * FP8BS_ERR_TIMEOUT (either word recorded a timeout) or FP8BS_ERR_CUDA.
  */
