@@ -54,11 +54,19 @@ struct SmallLayout {
     static constexpr int SCL_OFF = RING;
     static constexpr int SLOT = BNT * 4 + 16;            // one K block's column scales + s_w
     static constexpr int BAR_OFF = SCL_OFF + SM_SLOTS * SLOT;
-    // full[S], empty[S], tfull[2], tempty[2], drain, sfull[SLOTS], sempty[SLOTS]
-    static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * SM_SLOTS;
+    // TMEM accumulators of BNT columns: as many as fit in half (32 tokens) or all (64, 128) of
+    // the 512 columns, so that the MMAs run up to NBUF K blocks ahead of the epilogue and the
+    // hand-over of a block's partial is hidden behind the weight stream (one in the serial build)
+#ifdef FP8BS_SERIAL_PIPELINE
+    static constexpr int NBUF = 1;
+#else
+    static constexpr int NBUF = BNT <= 64 ? 8 : 4;
+#endif
+    static constexpr uint32_t TMEM_COLS = NBUF * BNT;    // 256 or 512 (serial: BNT)
+    // full[S], empty[S], tfull[NBUF], tempty[NBUF], drain, sfull[SLOTS], sempty[SLOTS]
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * NBUF + 1 + 2 * SM_SLOTS;
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int BYTES = MISC_OFF + 16 + SM_ALIGN;
-    static constexpr uint32_t TMEM_COLS = 2 * BNT;       // two accumulators; 64, 128 or 256
 };
 
 __device__ __forceinline__ void raise_small(int* err, uint32_t abort_addr, int code)
@@ -133,8 +141,8 @@ gemm_small_kernel(const __grid_constant__ CUtensorMap map_w,
     const uint32_t full0 = base + L::BAR_OFF;
     const uint32_t empty0 = full0 + 8 * L::STAGES;
     const uint32_t tfull0 = empty0 + 8 * L::STAGES;
-    const uint32_t tempty0 = tfull0 + 16;
-    const uint32_t drain_bar = tempty0 + 16;
+    const uint32_t tempty0 = tfull0 + 8 * L::NBUF;
+    const uint32_t drain_bar = tempty0 + 8 * L::NBUF;
     const uint32_t sfull0 = drain_bar + 8;
     const uint32_t sempty0 = sfull0 + 8 * SM_SLOTS;
     const uint32_t scl0 = base + L::SCL_OFF;
@@ -159,7 +167,7 @@ gemm_small_kernel(const __grid_constant__ CUtensorMap map_w,
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, 1);
         }
-        for (int b = 0; b < 2; b++) {
+        for (int b = 0; b < L::NBUF; b++) {
             mbar_init(tfull0 + 8 * b, 1);
             mbar_init(tempty0 + 8 * b, SM_EPI_WARPS);
         }
@@ -216,8 +224,8 @@ gemm_small_kernel(const __grid_constant__ CUtensorMap map_w,
             uint32_t it = 0;
             bool issued = false;
             for (int kb = kb0; kb < kb1; kb++, it++) {
-                const uint32_t b = it & 1u;
-                if (!mbar_wait(tempty0 + 8 * b, ((it >> 1) & 1u) ^ 1u, abort_addr, budget)) {
+                const uint32_t b = it % L::NBUF;
+                if (!mbar_wait(tempty0 + 8 * b, ((it / L::NBUF) & 1u) ^ 1u, abort_addr, budget)) {
                     raise_small(p.err, abort_addr, DEV_TIMEOUT_MMA_TMEM);
                     break;
                 }
@@ -296,8 +304,9 @@ gemm_small_kernel(const __grid_constant__ CUtensorMap map_w,
         for (int kb = kb0; kb < kb1; kb++, it++) {
             const uint32_t slot = it % SM_SLOTS;
             const bool sgot = mbar_wait(sfull0 + 8 * slot, (it / SM_SLOTS) & 1u, abort_addr, budget);
-            const uint32_t b = it & 1u;
-            const bool got = sgot && mbar_wait(tfull0 + 8 * b, (it >> 1) & 1u, abort_addr, budget);
+            const uint32_t b = it % L::NBUF;
+            const bool got =
+                sgot && mbar_wait(tfull0 + 8 * b, (it / L::NBUF) & 1u, abort_addr, budget);
             if (!__all_sync(0xffffffffu, got)) {
                 if (lane == 0) raise_small(p.err, abort_addr, DEV_TIMEOUT_EPILOGUE);
                 break;
