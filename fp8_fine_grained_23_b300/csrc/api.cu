@@ -193,7 +193,7 @@ int dense_gemm_launch(DeviceInfo* d, int* err, GemmKind kind, const uint8_t* a_q
         sa.err = err;
         sa.budget = wait_budget();
         return cuda_status(launch_gemm_small(mw, ma, sa, bnt, out_dtype == FP8BS_OUT_F32,
-                                             reinterpret_cast<cudaStream_t>(stream)));
+                                             d->num_sms, reinterpret_cast<cudaStream_t>(stream)));
     }
 
     const int cluster = gemm_cluster_size(false);

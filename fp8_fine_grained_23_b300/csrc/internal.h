@@ -89,9 +89,11 @@ struct SmallArgs {
     long long budget;
 };
 constexpr int GEMM_SMALL_MAX_M = 64;   // above this the tiled CTA-pair kernel is faster
-int gemm_small_tokens(int64_t M);   // tokens per tile for M rows: 32 or 64 (128 kept for tests)
+int gemm_small_tokens(int64_t M);   // tokens per tile for M rows: 32 or 64
+// max_ctas: the persistent grid's upper bound when the K loop is not split (the SM count)
 cudaError_t launch_gemm_small(const CUtensorMap& map_w, const CUtensorMap& map_a,
-                              const SmallArgs& args, int bnt, bool out_f32, cudaStream_t stream);
+                              const SmallArgs& args, int bnt, bool out_f32, int max_ctas,
+                              cudaStream_t stream);
 
 // DENSE: per-128x128-block B scales; GROUPED: the same per expert; ROW_SCALED: a scale per B
 // row and K block (the 1d1d weight-gradient GEMM), dense only.

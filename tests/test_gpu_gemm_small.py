@@ -2,8 +2,9 @@
 cores, with the K loop split over a cluster of up to 8 CTAs when the weight tiles are few)
 against the oracle, within |gpu - oracle| <= 1e-5 * sum|a_hat w_hat| + 1 ulp of the output type.
 The shapes pick every split factor (1, 2, 4, 8), token tiles of 32 and 64, ragged N and K, the
-decode-size versions of the dense and MLA projections, and sizes on both sides of the switch to
-the tiled CTA-pair kernel (M = 64 / 65, 100, 128)."""
+decode-size versions of the dense and MLA projections, unsplit problems with more weight tiles
+than SMs (the persistent grid takes two or three tiles per CTA), and sizes on both sides of the
+switch to the tiled CTA-pair kernel (M = 64 / 65, 100, 128)."""
 import numpy as np
 import pytest
 import torch
@@ -43,7 +44,9 @@ def run(F, M, N, K, out_dtype, seed):
     (65, 384, 256),       # first size on the tiled kernel
     (100, 1040, 384),     # ragged N, 3 K blocks, token tile 128
     (128, 256, 128),      # one K block
-    (7, 24576, 1536),     # MLA q-up at decode size: 192 tiles
+    (7, 24576, 1536),     # MLA q-up at decode size: 192 tiles, up to two per CTA
+    (17, 38400, 384),     # 300 tiles: up to three per CTA, token tile 32
+    (40, 40960, 256),     # 320 tiles: up to three per CTA, token tile 64, ragged M
 ])
 @pytest.mark.parametrize("out", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
 def test_few_rows(F, M, N, K, out):

@@ -1,10 +1,10 @@
 """Parity of the serialised-pipeline debug build (libfp8bs_serial.so, `build.py --serial`).
 
 That build runs every pipelined kernel with the shallowest pipeline its structure allows: one
-operand stage, one scale slot and one TMEM accumulator in the tiled GEMMs, and the fewest stages
-that hold the partial tile in the few-row GEMM. Every role then waits for the previous one at every step, so a barrier that is
-missing, waited on with the wrong phase or arrived on too early shows up as a different result
-or a timeout. The same small and ragged parity checks as the regular build run here against
+operand stage, one scale slot and one TMEM accumulator in the tiled GEMMs, one operand stage and
+one TMEM accumulator in the few-row GEMM. Every role then waits for the previous one at every
+step, so a barrier that is missing, waited on with the wrong phase or arrived on too early shows
+up as a different result or a timeout. The same small and ragged parity checks as the regular build run here against
 the oracle (quantizer codes and scales bit-exact, GEMMs within 1e-5 * sum|a_k w_k| + 1 ulp).
 """
 import ctypes
@@ -58,8 +58,11 @@ def test_serial_tiny_workload(FS, out_dtype):
     GM.check_full(FS, a, w, out_dtype)
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 16, 128), (16, 1536, 1024), (64, 272, 384),
-                                   (65, 400, 512), (257, 400, 1024), (383, 1040, 256)])
+# few-row kernel: one tile; split K over 2 CTAs; 300 tiles on the persistent grid (two or three
+# per CTA); token tile 64; then the tiled kernel
+@pytest.mark.parametrize("M,N,K", [(1, 16, 128), (16, 1536, 1024), (16, 38400, 256),
+                                   (64, 272, 384), (65, 400, 512), (257, 400, 1024),
+                                   (383, 1040, 256)])
 def test_serial_ragged_gemm(FS, M, N, K):
     g = W.generator(900 + M + N, "cpu")
     a = W.activations(M, K, g, "cpu")
