@@ -107,7 +107,10 @@ int fp8_quant_weight_128x128_ue8m0(const void *w, int64_t N, int64_t K, int64_t 
  *   P[m][n][kb] = sum over k in [128 kb, 128 kb + 128) of decode(a_q[m][k]) * decode(w_q[n][k]).
  * Each P is formed by the tensor cores in FP32 and promoted once per 128-wide K block: it is
  * multiplied by the FP32 product of its two scales and added to an FP32 accumulator with one
- * fused multiply-add. The accumulation order over K blocks is increasing kb.
+ * fused multiply-add. The accumulation order over K blocks is increasing kb. For M <= 64, when the
+ * weight row tiles are too few to occupy the GPU, the K loop is cut into 2, 4 or 8 contiguous
+ * ranges, each accumulated that way from zero, and their FP32 sums are added in range order; the
+ * result depends only on M, N and K and the GPU's SM count (no atomics, deterministic).
  *   a_q  E4M3 [M][K] (contiguous rows), a_s FP32 [K/128][M]   (fp8_quant_act_1x128 layout)
  *   w_q  E4M3 [N][K] (contiguous rows), w_s FP32 [ceil(N/128)][K/128] (weight-quantizer layout)
  *   c    [M][ldc] of BF16 (out_dtype FP8BS_OUT_BF16, round to nearest even) or FP32.
