@@ -111,6 +111,20 @@ int make_code_map(CUtensorMap* map, const void* base, int64_t cols, int64_t rows
     return r == CUDA_SUCCESS ? FP8BS_OK : FP8BS_ERR_CUDA;
 }
 
+int make_out_map(CUtensorMap* map, void* c, int64_t cols, int64_t rows, int64_t ld, bool f32)
+{
+    const int64_t elem = f32 ? 4 : 2;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld * elem)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(64 / elem), 32u};
+    const cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = g_encode(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          2, c, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FP8BS_OK : FP8BS_ERR_CUDA;
+}
+
 int check_quant_args(const void* in, int64_t rows, int64_t K, int64_t ld_in, const void* q,
                      int64_t ldq, const void* scales)
 {
@@ -197,9 +211,13 @@ int dense_gemm_launch(DeviceInfo* d, int* err, GemmKind kind, const uint8_t* a_q
     }
 
     const int cluster = gemm_cluster_size(false);
-    CUtensorMap ma, mb;
+    CUtensorMap ma, mb, mc;
     if ((st = make_code_map(&ma, a_q, K, M, K, GEMM_BM)) != FP8BS_OK) return st;
     if ((st = make_code_map(&mb, w_q, K, N, K, GEMM_BN / cluster)) != FP8BS_OK) return st;
+    if (kind == GemmKind::DENSE_QUANT)
+        mc = ma;   // (the re-quantized output stores its codes itself)
+    else if ((st = make_out_map(&mc, c, N, M, ldc, out_dtype == FP8BS_OUT_F32)) != FP8BS_OK)
+        return st;
 
     GemmArgs args{};
     args.a_s = a_s;
@@ -222,7 +240,7 @@ int dense_gemm_launch(DeviceInfo* d, int* err, GemmKind kind, const uint8_t* a_q
     args.err = err;
     args.budget = wait_budget();
     args.fault_skip_release = -1;
-    return cuda_status(launch_gemm(ma, mb, args, kind, out_dtype == FP8BS_OUT_F32, d->num_sms,
+    return cuda_status(launch_gemm(ma, mb, mc, args, kind, out_dtype == FP8BS_OUT_F32, d->num_sms,
                                    reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -257,9 +275,13 @@ int grouped_gemm(GemmKind kind, const uint8_t* a_q, const float* a_s, const uint
     if ((st = ensure_error_word(d)) != FP8BS_OK) return st;
     if ((st = ensure_encoder()) != FP8BS_OK) return st;
 
-    CUtensorMap ma, mb;
+    CUtensorMap ma, mb, mc;
     if ((st = make_code_map(&ma, a_q, K, R, K, GEMM_BM)) != FP8BS_OK) return st;
     if ((st = make_code_map(&mb, w_q, K, G * N, K, GEMM_BN)) != FP8BS_OK) return st;
+    if (kind == GemmKind::GROUPED_SWIGLU)
+        mc = ma;   // (the fused epilogue stores its codes itself)
+    else if ((st = make_out_map(&mc, c, N, R, ldc, out_f32)) != FP8BS_OK)
+        return st;
 
     GemmArgs args{};
     args.a_s = a_s;
@@ -286,7 +308,7 @@ int grouped_gemm(GemmKind kind, const uint8_t* a_q, const float* a_s, const uint
     if (bound > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
     const int max_ctas = static_cast<int>(bound < d->num_sms ? bound : d->num_sms);
     return cuda_status(
-        launch_gemm(ma, mb, args, kind, out_f32, max_ctas, reinterpret_cast<cudaStream_t>(stream)));
+        launch_gemm(ma, mb, mc, args, kind, out_f32, max_ctas, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 // The two tile quantizers, with amax/448 or power-of-two (ue8m0) scales.

@@ -262,13 +262,18 @@ __device__ __forceinline__ void st_v4(void* p, uint32_t a, uint32_t b, uint32_t 
 template <bool GROUPED, bool OUT_F32, bool PAIR, bool RS, bool SW, bool QO = false>
 __global__ void __launch_bounds__(THREADS, 1)
 fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
-                            const __grid_constant__ CUtensorMap map_b, const GemmArgs p)
+                            const __grid_constant__ CUtensorMap map_b,
+                            const __grid_constant__ CUtensorMap map_c, const GemmArgs p)
 {
     using L = Layout<GROUPED, PAIR, RS, SW>;
     static_assert(!SW || (GROUPED && !PAIR && !RS && !OUT_F32), "SwiGLU epilogue: grouped only");
     static_assert(!QO || (!GROUPED && !RS && !SW && !OUT_F32), "re-quantized output: dense only");
     constexpr int STAGES = L::STAGES;
     constexpr int CL = L::CL;
+    // Output stores through the TMA engine (see the store below): the dense kernels with BF16
+    // output and the row-scaled one. The plain dense kernel with FP32 output keeps 32-column
+    // TMEM chunks and plain stores (with the bulk path it spilled and ran 23% slower).
+    constexpr bool BULK_STORE = !GROUPED && !SW && !QO && (RS || !OUT_F32);
     // Odd-CTA epilogue warps release TMEM straight to the even CTA (2% faster than forwarding
     // through the odd CTA's MMA warp); the row-scaled epilogue keeps the forwarding, which costs
     // it no registers (the remote address spills there).
@@ -638,11 +643,12 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                             ffma2(acc[8 * (c + 1) + i],
                                   fmul2(u1[i], ld_shared_u64(sb + 64 * (c + 1) + 8 * i)), sc2);
                     }
-                } else if constexpr (SW || QO) {
+                } else if constexpr (SW || QO || BULK_STORE) {
                     // SW: gate columns 64 half .. + 63 into acc[0..31] (scale s_a * s_w[gate
                     // block]), up columns 128 + 64 half .. + 63 into acc[32..63] (s_a * s_w[up
-                    // block]); QO: the usual 128 columns, one scale. 16-column chunks leave
-                    // registers for the tail that follows the K loop.
+                    // block]); otherwise the usual 128 columns, one scale. 16-column chunks
+                    // leave registers for the tail that follows the K loop (the fused tails, and
+                    // the dense kernel's bulk output stores).
                     auto col = [](int c) -> uint32_t {
                         return (SW && c >= 4) ? 128 + 16 * (c - 4) : 16 * c;
                     };
@@ -662,6 +668,7 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                             ffma2(acc[8 * (c + 1) + i], u1[i], c + 1 < 4 ? sc2 : sc2b);
                     }
                 } else {
+                    // four 32-column chunks
                     uint64_t v0[16], v1[16];
                     tmem_ld_32cols(taddr, v0);
                     tmem_wait_ld(v0);
@@ -813,10 +820,16 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                 continue;
             }
 
-            // Store: stage this warp's 32 rows x 64 B at a time in shared memory, chunk j (16 B)
-            // of row r at position (j + r/2) % 4, which keeps both the row-wise writes and the
-            // column-wise reads free of bank conflicts; then write 8 rows of 64 contiguous bytes
-            // per warp instruction instead of 32 scattered 16-byte pieces.
+            // Store: this warp's 32 rows go out 64 bytes of each row at a time, staged in a 2 KB
+            // shared buffer: chunk j (16 B) of row r at position j ^ ((r / 2) % 4), which keeps
+            // the row-wise writes here and the column-wise reads below free of bank conflicts.
+            // BULK_STORE: the staged buffer is the output map's box (that position is its 64-byte
+            // swizzle); one lane hands it to the TMA engine and the warp goes on, waiting only
+            // for the engine to have read the buffer before refilling it, so the global writes
+            // overlap the next tile's K loop. Otherwise plain row-predicated stores, 8 rows of 64
+            // bytes per instruction: grouped (rows past a group's end belong to the next group's
+            // output, which the map cannot clip; bulk stores also measured 3-4% slower on the
+            // HBM-bound grouped shapes) and dense FP32.
             {
                 constexpr int ELEM = OUT_F32 ? 4 : 2;
                 constexpr int GCOLS = 64 / ELEM;             // columns per 64-byte staged row
@@ -824,8 +837,12 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     decode_tile<GROUPED, CL>(t, p, s_tstart, s_off, static_cast<int>(crank));
                 const uint32_t stg = base + L::STG_OFF + (warp - EPI_WARP0) * STG_WARP_BYTES;
                 const int64_t wrow0 = ts.row0 + quad * 32;   // first row of this warp
+                // (rows past M are outside the output map and not written)
+                constexpr bool bulk = BULK_STORE;
 #pragma unroll
                 for (int g = 0; g < 128 / GCOLS; g++) {
+                    if (bulk && lane == 0) bulk_wait_group_read<0>();   // its last box was read
+                    __syncwarp();
 #pragma unroll
                     for (int jc = 0; jc < 4; jc++) {
                         uint4 v;
@@ -840,24 +857,38 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                                            pack_bf16x2(f32x2_lo(acc[q + 2]), f32x2_hi(acc[q + 2])),
                                            pack_bf16x2(f32x2_lo(acc[q + 3]), f32x2_hi(acc[q + 3])));
                         }
-                        st_shared_v4(stg + lane * 64 + (((jc + (lane >> 1)) & 3) * 16), v);
+                        st_shared_v4(stg + lane * 64 + ((jc ^ ((lane >> 1) & 3)) * 16), v);
                     }
-                    __syncwarp();
-                    const int ch = lane & 3;
-                    const int gcol = ncol0 + g * GCOLS + ch * (16 / ELEM);
+                    const int gcol0 = ncol0 + g * GCOLS;
+                    if (bulk) {
+                        fence_proxy_async_smem();            // the box is visible to the engine
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(&map_c, stg, gcol0, static_cast<int32_t>(wrow0));
+                            bulk_commit_group();
+                        }
+                    } else {
+                        __syncwarp();
+                        const int ch = lane & 3;
+                        const int gcol = gcol0 + ch * (16 / ELEM);
 #pragma unroll
-                    for (int i = 0; i < 4; i++) {
-                        const int rr = i * 8 + (lane >> 2);
-                        const uint4 v = ld_shared_v4(stg + rr * 64 + (((ch + (rr >> 1)) & 3) * 16));
-                        const int64_t grow = wrow0 + rr;
-                        if (grow >= 0 && grow < ts.row_end && gcol < p.N)
-                            st_v4(static_cast<uint8_t*>(p.c) + (grow * p.ldc + gcol) * ELEM, v.x, v.y,
-                                  v.z, v.w);
+                        for (int i = 0; i < 4; i++) {
+                            const int rr = i * 8 + (lane >> 2);
+                            const uint4 v = ld_shared_v4(stg + rr * 64 + ((ch ^ ((rr >> 1) & 3)) * 16));
+                            const int64_t grow = wrow0 + rr;
+                            if (grow >= 0 && grow < ts.row_end && gcol < p.N)
+                                st_v4(static_cast<uint8_t*>(p.c) + (grow * p.ldc + gcol) * ELEM, v.x,
+                                      v.y, v.z, v.w);
+                        }
+                        __syncwarp();
                     }
-                    __syncwarp();
                 }
             }
         }
+        // every output box this warp handed to the TMA engine has been written before the
+        // CTA may finish
+        if (lane == 0) bulk_wait_group<0>();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -873,8 +904,8 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
 }
 
 template <bool GROUPED, bool OUT_F32, bool PAIR, bool RS, bool SW = false, bool QO = false>
-cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& args,
-                       int max_ctas, cudaStream_t stream)
+cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
+                       const GemmArgs& args, int max_ctas, cudaStream_t stream)
 {
     constexpr int CL = PAIR ? 2 : 1;
     auto kern = fp8_blockscaled_gemm_kernel<GROUPED, OUT_F32, PAIR, RS, SW, QO>;
@@ -910,7 +941,7 @@ cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const GemmA
     if (!GROUPED && args.num_tiles < clusters) clusters = args.num_tiles;
     if (clusters < 1) clusters = 1;
     cfg.gridDim = dim3(static_cast<unsigned>(clusters * CL));
-    e = cudaLaunchKernelEx(&cfg, kern, ma, mb, args);
+    e = cudaLaunchKernelEx(&cfg, kern, ma, mb, mc, args);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -958,26 +989,27 @@ int gemm_band(int mgroups, int NT, int64_t K, int clusters)
     return b < mgroups ? b : mgroups;
 }
 
-cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args,
-                        GemmKind kind, bool out_f32, int max_ctas, cudaStream_t stream)
+cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b,
+                        const CUtensorMap& map_c, const GemmArgs& args, GemmKind kind,
+                        bool out_f32, int max_ctas, cudaStream_t stream)
 {
     constexpr bool DP = GEMM_DENSE_CLUSTER == 2;
     switch (kind) {
     case GemmKind::GROUPED:
-        return out_f32 ? launch_one<true, true, false, false>(map_a, map_b, args, max_ctas, stream)
-                       : launch_one<true, false, false, false>(map_a, map_b, args, max_ctas, stream);
+        return out_f32 ? launch_one<true, true, false, false>(map_a, map_b, map_c, args, max_ctas, stream)
+                       : launch_one<true, false, false, false>(map_a, map_b, map_c, args, max_ctas, stream);
     case GemmKind::GROUPED_SWIGLU:
-        return launch_one<true, false, false, false, true>(map_a, map_b, args, max_ctas, stream);
+        return launch_one<true, false, false, false, true>(map_a, map_b, map_c, args, max_ctas, stream);
     case GemmKind::DENSE_QUANT:
-        return launch_one<false, false, DP, false, false, true>(map_a, map_b, args, max_ctas,
+        return launch_one<false, false, DP, false, false, true>(map_a, map_b, map_c, args, max_ctas,
                                                                 stream);
     case GemmKind::ROW_SCALED:
-        return out_f32 ? launch_one<false, true, DP, true>(map_a, map_b, args, max_ctas, stream)
-                       : launch_one<false, false, DP, true>(map_a, map_b, args, max_ctas, stream);
+        return out_f32 ? launch_one<false, true, DP, true>(map_a, map_b, map_c, args, max_ctas, stream)
+                       : launch_one<false, false, DP, true>(map_a, map_b, map_c, args, max_ctas, stream);
     case GemmKind::DENSE:
     default:
-        return out_f32 ? launch_one<false, true, DP, false>(map_a, map_b, args, max_ctas, stream)
-                       : launch_one<false, false, DP, false>(map_a, map_b, args, max_ctas, stream);
+        return out_f32 ? launch_one<false, true, DP, false>(map_a, map_b, map_c, args, max_ctas, stream)
+                       : launch_one<false, false, DP, false>(map_a, map_b, map_c, args, max_ctas, stream);
     }
 }
 

@@ -101,8 +101,11 @@ cudaError_t launch_gemm_small(const CUtensorMap& map_w, const CUtensorMap& map_a
 // to E4M3 with 1x128 scales.
 // DENSE_QUANT: dense, output re-quantized to E4M3 codes with 1x128 scales.
 enum class GemmKind { DENSE, GROUPED, ROW_SCALED, GROUPED_SWIGLU, DENSE_QUANT };
-cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmArgs& args,
-                        GemmKind kind, bool out_f32, int max_ctas, cudaStream_t stream);
+// map_c: the output C as BF16 / FP32 with 64-byte boxes of 32 rows (make_out_map); read by the
+// kinds whose output is BF16 or FP32 (not GROUPED_SWIGLU or DENSE_QUANT, which take any map).
+cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b,
+                        const CUtensorMap& map_c, const GemmArgs& args, GemmKind kind,
+                        bool out_f32, int max_ctas, cudaStream_t stream);
 int gemm_cluster_size(bool grouped);
 // Dense tile order: m-groups (of cluster-size m-tiles) per band for a problem of `mgroups` x `NT`
 // items with K bytes of codes per row, on `clusters` concurrent clusters.
@@ -132,6 +135,9 @@ int ensure_error_word(DeviceInfo* d);
 int ensure_encoder();
 int make_code_map(CUtensorMap* map, const void* base, int64_t cols, int64_t rows, int64_t ld,
                   int box_rows);
+// The GEMM output [rows][ld] of BF16 or FP32 as a TMA store target: boxes of 64 bytes x 32 rows
+// with the 64-byte swizzle.
+int make_out_map(CUtensorMap* map, void* c, int64_t cols, int64_t rows, int64_t ld, bool f32);
 int check_quant_args(const void* in, int64_t rows, int64_t K, int64_t ld_in, const void* q,
                      int64_t ldq, const void* scales);
 int check_gemm_args(const void* a_q, const void* a_s, const void* w_q, const void* w_s,
