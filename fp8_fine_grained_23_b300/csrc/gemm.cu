@@ -75,6 +75,7 @@ constexpr int NUM_EPI_WARPS = 8;
 constexpr int PRODUCER_WARP = 0;
 constexpr int MMA_WARP = 1;
 constexpr int SCALE_WARP = 2;
+constexpr int STORE_WARP = 3;   // dense BF16 output: writes each staged output tile to C
 constexpr int EPI_WARP0 = 4;
 constexpr int THREADS = 384;
 constexpr int REGS_CONTROL = 72;           // warpgroup 0 after setmaxnreg.dec
@@ -111,16 +112,21 @@ struct Layout {
     static constexpr int CL = PAIR ? 2 : 1;              // CTAs per cluster
     static constexpr int B_PART = B_BYTES / CL;          // W rows held by this CTA
     static constexpr int STAGE = A_BYTES + B_PART;
-    static constexpr int STAGES = SERIAL ? 1 : (PAIR ? 6 : 4);
+    // (CTA pairs: 4 stages measured as fast as 6, which leaves room for a whole output tile)
+    static constexpr int STAGES = SERIAL ? 1 : 4;
     static constexpr int A_OFF = 0;
     static constexpr int B_OFF = STAGES * A_BYTES;
     static constexpr int STG_OFF = STAGES * STAGE;
-    static constexpr int SCL_OFF = STG_OFF + STG_BYTES;
+    // output staging: CTA pairs hold a whole BF16 output tile (4 boxes of 32 rows x 64 B per
+    // epilogue warp), the grouped kernel one box per warp
+    static constexpr int STG_SIZE = PAIR ? 4 * STG_BYTES : STG_BYTES;
+    static constexpr int SCL_OFF = STG_OFF + STG_SIZE;
     static constexpr int XCH_OFF = SCL_OFF + SCALE_SLOTS * SLOT;
     static constexpr int BAR_OFF = XCH_OFF + (SW ? 2 * 2 * 128 * 4 : 0);
     // full[S], empty[S], tfull[2], tempty[2], drain, sfull[SCALE_SLOTS], sempty[SCALE_SLOTS],
+    // ostaged, ofree (the output tile handed between the epilogue and the store warp),
     // SW: xch[4] (one per TMEM lane quarter)
-    static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * SCALE_SLOTS + (SW ? 4 : 0);
+    static constexpr int NUM_BARS = 2 * STAGES + 7 + 2 * SCALE_SLOTS + (SW ? 4 : 0);
     static constexpr int MISC_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int GROUP_OFF = MISC_OFF + 16;
     static_assert(A_BYTES % 1024 == 0 && B_PART % 1024 == 0, "tiles keep 1024-byte alignment");
@@ -259,7 +265,9 @@ __device__ __forceinline__ void st_v4(void* p, uint32_t a, uint32_t b, uint32_t 
 }
 
 // QO: the output re-quantized to E4M3 in 1x128 tiles (codes to p.c, scales to p.h_s).
-template <bool GROUPED, bool OUT_F32, bool PAIR, bool RS, bool SW, bool QO = false>
+// DEFER: output tiles written by the store warp (dense BF16 output only).
+template <bool GROUPED, bool OUT_F32, bool PAIR, bool RS, bool SW, bool QO = false,
+          bool DEFER = false>
 __global__ void __launch_bounds__(THREADS, 1)
 fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                             const __grid_constant__ CUtensorMap map_b,
@@ -274,6 +282,12 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     // output and the row-scaled one. The plain dense kernel with FP32 output keeps 32-column
     // TMEM chunks and plain stores (with the bulk path it spilled and ran 23% slower).
     constexpr bool BULK_STORE = !GROUPED && !SW && !QO && (RS || !OUT_F32);
+    // DEFER (dense BF16 output, chosen by the host for long K loops and several tiles per pair):
+    // the epilogue stages a finished tile whole in shared memory and goes on to the next tile at
+    // once; the store warp writes the staged tile to C meanwhile. (One warp needs ~2 us for a
+    // tile: with short K loops it fell behind, and a pair's last tile waited for it.)
+    constexpr bool DEFER_STORE = DEFER;
+    static_assert(!DEFER || (BULK_STORE && PAIR && !RS && !OUT_F32), "store warp: dense BF16");
     // Odd-CTA epilogue warps release TMEM straight to the even CTA (2% faster than forwarding
     // through the odd CTA's MMA warp); the row-scaled epilogue keeps the forwarding, which costs
     // it no registers (the remote address spills there).
@@ -293,7 +307,9 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     const uint32_t drain_bar = tempty0 + 16;
     const uint32_t sfull0 = drain_bar + 8;
     const uint32_t sempty0 = sfull0 + 8 * SCALE_SLOTS;
-    const uint32_t xch0 = sempty0 + 8 * SCALE_SLOTS;   // SW only
+    const uint32_t ostaged = sempty0 + 8 * SCALE_SLOTS;   // DEFER_STORE only
+    const uint32_t ofree = ostaged + 8;                   // DEFER_STORE only
+    const uint32_t xch0 = ofree + 8;                      // SW only
     const uint32_t scl0 = base + L::SCL_OFF;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + L::MISC_OFF);
     const uint32_t abort_addr = base + L::MISC_OFF + 4;   // shared word: a role gave up
@@ -324,6 +340,10 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
         for (int i = 0; i < SCALE_SLOTS; i++) {
             mbar_init(sfull0 + 8 * i, 32);              // one cp.async completion per loader lane
             mbar_init(sempty0 + 8 * i, NUM_EPI_WARPS);
+        }
+        if constexpr (DEFER_STORE) {
+            mbar_init(ostaged, NUM_EPI_WARPS);   // every epilogue warp has staged its rows
+            mbar_init(ofree, 1);                 // the store warp has read the staged tile
         }
         if constexpr (SW) {
             for (int q = 0; q < 4; q++) mbar_init(xch0 + 8 * q, 2);   // the two warps of a quad
@@ -558,6 +578,45 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                                    budget))
                         atomicCAS(p.err, 0, DEV_TIMEOUT_DRAIN);
             }
+        } else if (DEFER_STORE && warp == STORE_WARP) {
+            // ---------------------------------------------------------------- store warp
+            // Each staged output tile goes to C, 8 rows of 64 contiguous bytes per store
+            // instruction (row- and column-predicated), while the epilogue works on the next
+            // tile; then the staging buffer is handed back.
+            uint32_t n = 0;
+            const int ch = lane & 3;
+            for (int t = cluster_id; t < num_tiles; t += num_clusters, n++) {
+                const bool got = mbar_wait(ostaged, n & 1u, abort_addr, budget);
+                if (!__all_sync(0xffffffffu, got)) {
+                    if (lane == 0) raise_error(p.err, abort_addr, DEV_TIMEOUT_EPILOGUE);
+                    break;
+                }
+                const TileInfo ts =
+                    decode_tile<GROUPED, CL>(t, p, s_tstart, s_off, static_cast<int>(crank));
+#pragma unroll 1
+                for (int w = 0; w < NUM_EPI_WARPS; w++) {
+                    // epilogue warp EPI_WARP0 + w: TMEM lane quarter w % 4, column half w / 4
+                    const uint32_t buf = base + L::STG_OFF + w * 4 * STG_WARP_BYTES;
+                    const int64_t wrow0 = ts.row0 + (w & 3) * 32;
+                    const int col0 = ts.n0 + (w >> 2) * 128;
+#pragma unroll
+                    for (int g = 0; g < 4; g++) {
+                        const int gcol = col0 + g * 32 + ch * 8;
+#pragma unroll
+                        for (int i = 0; i < 4; i++) {
+                            const int rr = i * 8 + (lane >> 2);
+                            const uint4 v = ld_shared_v4(buf + g * STG_WARP_BYTES + rr * 64 +
+                                                         ((ch ^ ((rr >> 1) & 3)) * 16));
+                            const int64_t grow = wrow0 + rr;
+                            if (grow < ts.row_end && gcol < p.N)
+                                st_v4(static_cast<uint8_t*>(p.c) + (grow * p.ldc + gcol) * 2, v.x,
+                                      v.y, v.z, v.w);
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ofree);
+            }
         }
     } else {
         regs_inc<REGS_EPILOGUE>();
@@ -572,6 +631,8 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
         uint32_t j = 0;
         uint64_t acc[64];   // 128 FP32 accumulators as packed pairs (columns 2i, 2i + 1)
         uint32_t tile_n = 0;   // tiles finished by this CTA (SW: parity of the exchange buffers)
+        // DEFER_STORE: this warp's part of the staged output tile (32 rows x 128 columns)
+        const uint32_t d_buf = base + L::STG_OFF + (warp - EPI_WARP0) * 4 * STG_WARP_BYTES;
 
         for (int t = cluster_id; t < num_tiles; t += num_clusters, tile_n++) {
             const int ncol0 =
@@ -706,6 +767,7 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     else
                         mbar_arrive(tempty0 + 8 * b);
                 }
+
             }
             if (!ok) break;
 
@@ -820,6 +882,36 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                 continue;
             }
 
+            if constexpr (DEFER_STORE) {
+                // Once the store warp has read the previous staged tile, this warp stages its 32
+                // rows x 128 columns in four 2 KB blocks of 32 rows x 64 B (chunk j of row r at
+                // position j ^ ((r / 2) % 4), conflict-free both ways) and goes on to the next
+                // tile; the store warp writes them out meanwhile.
+                const bool freed = mbar_wait(ofree, (tile_n & 1u) ^ 1u, abort_addr, budget);
+                if (!__all_sync(0xffffffffu, freed)) {
+                    if (lane == 0) raise_error(p.err, abort_addr, DEV_TIMEOUT_EPILOGUE);
+                    break;
+                }
+#pragma unroll
+                for (int g = 0; g < 4; g++) {
+#pragma unroll
+                    for (int jc = 0; jc < 4; jc++) {
+                        const int q = g * 16 + jc * 4;
+                        const uint4 v =
+                            make_uint4(pack_bf16x2(f32x2_lo(acc[q]), f32x2_hi(acc[q])),
+                                       pack_bf16x2(f32x2_lo(acc[q + 1]), f32x2_hi(acc[q + 1])),
+                                       pack_bf16x2(f32x2_lo(acc[q + 2]), f32x2_hi(acc[q + 2])),
+                                       pack_bf16x2(f32x2_lo(acc[q + 3]), f32x2_hi(acc[q + 3])));
+                        st_shared_v4(d_buf + g * STG_WARP_BYTES + lane * 64 +
+                                         ((jc ^ ((lane >> 1) & 3)) * 16),
+                                     v);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ostaged);
+                continue;
+            }
+
             // Store: this warp's 32 rows go out 64 bytes of each row at a time, staged in a 2 KB
             // shared buffer: chunk j (16 B) of row r at position j ^ ((r / 2) % 4), which keeps
             // the row-wise writes here and the column-wise reads below free of bank conflicts.
@@ -903,12 +995,13 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     if constexpr (PAIR) cluster_sync();   // no CTA leaves while its peer still deallocates
 }
 
-template <bool GROUPED, bool OUT_F32, bool PAIR, bool RS, bool SW = false, bool QO = false>
+template <bool GROUPED, bool OUT_F32, bool PAIR, bool RS, bool SW = false, bool QO = false,
+          bool DEFER = false>
 cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
                        const GemmArgs& args, int max_ctas, cudaStream_t stream)
 {
     constexpr int CL = PAIR ? 2 : 1;
-    auto kern = fp8_blockscaled_gemm_kernel<GROUPED, OUT_F32, PAIR, RS, SW, QO>;
+    auto kern = fp8_blockscaled_gemm_kernel<GROUPED, OUT_F32, PAIR, RS, SW, QO, DEFER>;
     const size_t smem = gemm_smem_bytes(
         SW ? GemmKind::GROUPED_SWIGLU
            : (RS ? GemmKind::ROW_SCALED : (GROUPED ? GemmKind::GROUPED : GemmKind::DENSE)),
@@ -991,7 +1084,7 @@ int gemm_band(int mgroups, int NT, int64_t K, int clusters)
 
 cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b,
                         const CUtensorMap& map_c, const GemmArgs& args, GemmKind kind,
-                        bool out_f32, int max_ctas, cudaStream_t stream)
+                        bool out_f32, int max_ctas, cudaStream_t stream, bool store_warp)
 {
     constexpr bool DP = GEMM_DENSE_CLUSTER == 2;
     switch (kind) {
@@ -1008,8 +1101,12 @@ cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b,
                        : launch_one<false, false, DP, true>(map_a, map_b, map_c, args, max_ctas, stream);
     case GemmKind::DENSE:
     default:
-        return out_f32 ? launch_one<false, true, DP, false>(map_a, map_b, map_c, args, max_ctas, stream)
-                       : launch_one<false, false, DP, false>(map_a, map_b, map_c, args, max_ctas, stream);
+        if (out_f32)
+            return launch_one<false, true, DP, false>(map_a, map_b, map_c, args, max_ctas, stream);
+        if (store_warp)
+            return launch_one<false, false, DP, false, false, false, true>(map_a, map_b, map_c, args,
+                                                                          max_ctas, stream);
+        return launch_one<false, false, DP, false>(map_a, map_b, map_c, args, max_ctas, stream);
     }
 }
 

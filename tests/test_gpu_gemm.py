@@ -130,6 +130,39 @@ def test_full_size_dense_sampled(F):
     sampled_check(F, W.DENSE)
 
 
+def store_warp_case(F):
+    """A ragged shape with K loops of 32 blocks and 304 tiles for 74 CTA pairs: the launch the
+    host gives the store-warp variant (BF16 output written by a dedicated warp from a staged
+    tile). Returns (a, w, BF16 result, FP32 result)."""
+    M, N, K = 4000, 4752, 4096
+    g = W.generator(4242, "cuda")
+    a = W.activations(M, K, g, "cuda")
+    w = W.weights(N, K, g, "cuda")
+    aq, a_s = F.fp8_quant_act_1x128(a)
+    wq, w_s = F.fp8_quant_weight_128x128(w)
+    c16 = F.fp8_blockscaled_gemm(aq, a_s, wq, w_s, out_dtype=torch.bfloat16)
+    c32 = F.fp8_blockscaled_gemm(aq, a_s, wq, w_s, out_dtype=torch.float32)
+    assert F.fp8bs_last_error() == F.FP8BS_OK
+    return a, w, c16, c32
+
+
+def test_store_warp_variant(F):
+    """Every element: the BF16 output equals the FP32 output (another kernel variant, plain
+    stores) rounded to BF16, since both form the same FP32 sums; sampled rows and columns,
+    among them the ragged last ones, against the oracle."""
+    a, w, c16, c32 = store_warp_case(F)
+    assert torch.equal(c16, c32.to(torch.bfloat16))
+    M, N = c16.shape
+    rows = np.unique(np.concatenate([np.arange(0, M, 61), np.arange(M - 40, M)]))
+    cols = np.unique(np.concatenate([np.arange(0, N, 97), np.arange(N - 40, N)]))
+    pm, pn = np.repeat(rows, cols.size), np.tile(cols, rows.size)
+    qa, sa = oracle_quant_act(bits_of(a.cpu()))
+    qw, sw = oracle_quant_weight(bits_of(w.cpu()))
+    c64, cabs = oracle_points(qa, sa, qw, sw, pm, pn)
+    got = c16[torch.from_numpy(pm).cuda(), torch.from_numpy(pn).cuda()].float().cpu().numpy()
+    assert_within_tolerance(got, c64, cabs, "bf16", "store-warp 4000x4752x4096")
+
+
 def test_full_size_mla_sampled(F):
     for shape in W.MLA:
         sampled_check(F, shape)

@@ -70,6 +70,13 @@ def test_serial_ragged_gemm(FS, M, N, K):
     GM.check_full(FS, a, w, torch.bfloat16)
 
 
+def test_serial_store_warp_variant(FS):
+    """The store-warp variant (BF16 output of a long-K, many-tile launch) in the serial build:
+    equal to the FP32 output rounded to BF16, element by element."""
+    _, _, c16, c32 = GM.store_warp_case(FS)
+    assert torch.equal(c16, c32.to(torch.bfloat16))
+
+
 @pytest.mark.parametrize("counts,N,K", [([0, 1, 130, 37, 128], 144, 256),
                                         ([128, 256, 0, 1, 127, 129], 512, 384)])
 def test_serial_grouped(FS, counts, N, K):
