@@ -19,19 +19,23 @@
 //   warp 2     scale loader: per K block, cp.async copies of the tile's 128 activation scales
 //              and its two weight-block scales into an 8-slot shared-memory ring (sfull/sempty
 //              mbarriers), so the epilogue reads its scale from shared memory;
-//   warp 3     idle after set-up (warp 0 also builds the group table of the grouped variant);
-//              the grouped variant's tiles follow the group table built from device offsets;
+//   warp 3     store warp of the DEFER variant (dense BF16 output, long K loops): writes each
+//              output tile the epilogue staged in shared memory to C while the epilogue works
+//              on the next tile; idle otherwise (warp 0 also builds the group table of the
+//              grouped variant, whose tiles follow that table built from device offsets);
 //   warps 4-11 epilogue: warp w reads TMEM lanes 32*(w%4).. (its rows) and the 128 columns
-//              128*((w-4)/4).. (one weight block). Per K block it loads the partial in 32-column
-//              pieces (the next piece in flight while the current one is promoted) and promotes
-//              it into 128 FP32 registers per thread (packed pairs, fma.rn.f32x2). At the end of
-//              the tile the results go through a small shared-memory stage per warp and leave as
-//              whole 64-byte row segments (BF16 or FP32).
+//              128*((w-4)/4).. (one weight block). Per K block it loads the partial in 16- or
+//              32-column pieces (the next piece in flight while the current one is promoted)
+//              and promotes it into 128 FP32 registers per thread (packed pairs,
+//              fma.rn.f32x2). At the end of the tile the results are staged in shared memory as
+//              blocks of 32 rows x 64 bytes and leave as whole 64-byte row segments: through the
+//              store warp, as TMA bulk stores, or as plain stores (BF16 or FP32).
 //
 // The dense GEMM runs on CTA pairs (clusters of two, cta_group::2): the pair computes a 256x256
 // tile with one 256-row MMA per K step, issued by the even CTA. Each CTA loads only its own 128
-// A rows and 128 of the 256 W rows, so a K block brings 32 KB into each SM instead of 48 KB, and
-// a stage takes 32 KB, which leaves room for six. Both CTAs' loads complete on the even CTA's
+// A rows and 128 of the 256 W rows, so a K block brings 32 KB into each SM instead of 48 KB; a
+// stage takes 32 KB and four of them (as fast as six) leave room for a staged 64 KB output tile.
+// Both CTAs' loads complete on the even CTA's
 // `full` barrier; the MMA commits are multicast to both CTAs' `empty` and `tfull` barriers. The
 // epilogue warps of both CTAs release a TMEM buffer on the even CTA's `tempty` barrier (the odd
 // CTA's by remote arrives; in the row-scaled variant, whose epilogue has no register to spare,
@@ -49,12 +53,14 @@
 //        matching 64 up columns, forms silu(gate) * up, exchanges row maxima with the partner
 //        warp of its lane quarter and stores E4M3 codes with 1x128 scales;
 //   QO   (dense) the output re-quantized to E4M3 in 1x128 tiles: a thread's 128 columns are one
-//        tile, so amax, scale and codes are thread-local.
+//        tile, so amax, scale and codes are thread-local;
+//   DEFER (dense, BF16 output) output tiles written by the store warp (chosen by the host for K
+//        loops of 32+ blocks and 4+ tiles per pair; otherwise TMA bulk stores).
 // (Few rows of A, M <= 64, go to the swap-AB kernel in gemm_small.cu instead.)
 //
 // Registers: the launch gives 168 per thread (65536 / 384, rounded to 8). Warpgroup 0 drops to
 // 72 and the two epilogue warpgroups rise to 216 (128*72 + 256*216 = 384*168), which holds the
-// 128 accumulators and 64 staging registers of an epilogue thread.
+// 128 accumulators of an epilogue thread and its TMEM load registers (32 or 64).
 // Every mbarrier wait is bounded (clock budget); on expiry the CTA records an error code in the
 // device error word, stops issuing work, waits for its in-flight copies and MMAs, frees TMEM and
 // returns.
