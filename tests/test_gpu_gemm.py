@@ -153,6 +153,14 @@ def test_store_warp_variant(F):
     a, w, c16, c32 = store_warp_case(F)
     assert torch.equal(c16, c32.to(torch.bfloat16))
     M, N = c16.shape
+    # the same launch into rows of a wider buffer (ldc = N + 64): the 64 extra columns stay put
+    aq, a_s = F.fp8_quant_act_1x128(a)
+    wq, w_s = F.fp8_quant_weight_128x128(w)
+    wide = torch.full((M, N + 64), 3.0, dtype=torch.bfloat16, device="cuda")
+    F.fp8_blockscaled_gemm(aq, a_s, wq, w_s, out=wide[:, :N])
+    assert F.fp8bs_last_error() == F.FP8BS_OK
+    assert torch.equal(wide[:, :N], c16)
+    assert bool((wide[:, N:] == 3.0).all())
     rows = np.unique(np.concatenate([np.arange(0, M, 61), np.arange(M - 40, M)]))
     cols = np.unique(np.concatenate([np.arange(0, N, 97), np.arange(N - 40, N)]))
     pm, pn = np.repeat(rows, cols.size), np.tile(cols, rows.size)
