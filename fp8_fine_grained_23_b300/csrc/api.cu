@@ -234,9 +234,11 @@ int dense_gemm_launch(DeviceInfo* d, int* err, GemmKind kind, const uint8_t* a_q
     if (items > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
     args.num_tiles = static_cast<int>(items);
     args.band = gemm_band((args.MT + cluster - 1) / cluster, args.NT, K, d->num_sms / cluster);
-    // the store warp: BF16 dense output, K loops of at least 32 blocks, 4+ tiles per pair
-    const bool store_warp = kind == GemmKind::DENSE && out_dtype == FP8BS_OUT_BF16 &&
-                            args.KB >= 32 && items >= 4 * static_cast<int64_t>(d->num_sms / cluster);
+    // the store warp: BF16 dense output or re-quantized codes, K loops of at least 32 blocks,
+    // 4+ tiles per pair
+    const bool store_warp =
+        ((kind == GemmKind::DENSE && out_dtype == FP8BS_OUT_BF16) || kind == GemmKind::DENSE_QUANT) &&
+        args.KB >= 32 && items >= 4 * static_cast<int64_t>(d->num_sms / cluster);
     args.offsets = nullptr;
     args.h_s = c_s;
     args.G = 1;

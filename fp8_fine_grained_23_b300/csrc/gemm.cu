@@ -293,7 +293,11 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     // once; the store warp writes the staged tile to C meanwhile. (One warp needs ~2 us for a
     // tile: with short K loops it fell behind, and a pair's last tile waited for it.)
     constexpr bool DEFER_STORE = DEFER;
-    static_assert(!DEFER || (BULK_STORE && PAIR && !RS && !OUT_F32), "store warp: dense BF16");
+    static_assert(!DEFER || (PAIR && !GROUPED && !RS && !SW && !OUT_F32),
+                  "store warp: dense, BF16 output or E4M3 codes (QO)");
+    // the staged tile's element size, and its 32-row x 64-byte blocks per epilogue warp
+    constexpr int OUT_ELEM = QO ? 1 : 2;
+    constexpr int OUT_BLOCKS = 128 * OUT_ELEM / 64;
     // Odd-CTA epilogue warps release TMEM straight to the even CTA (2% faster than forwarding
     // through the odd CTA's MMA warp); the row-scaled epilogue keeps the forwarding, which costs
     // it no registers (the remote address spills there).
@@ -606,8 +610,8 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                     const int64_t wrow0 = ts.row0 + (w & 3) * 32;
                     const int col0 = ts.n0 + (w >> 2) * 128;
 #pragma unroll
-                    for (int g = 0; g < 4; g++) {
-                        const int gcol = col0 + g * 32 + ch * 8;
+                    for (int g = 0; g < OUT_BLOCKS; g++) {
+                        const int gcol = col0 + g * (64 / OUT_ELEM) + ch * (16 / OUT_ELEM);
 #pragma unroll
                         for (int i = 0; i < 4; i++) {
                             const int rr = i * 8 + (lane >> 2);
@@ -615,8 +619,8 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                                                          ((ch ^ ((rr >> 1) & 3)) * 16));
                             const int64_t grow = wrow0 + rr;
                             if (grow < ts.row_end && gcol < p.N)
-                                st_v4(static_cast<uint8_t*>(p.c) + (grow * p.ldc + gcol) * 2, v.x,
-                                      v.y, v.z, v.w);
+                                st_v4(static_cast<uint8_t*>(p.c) + (grow * p.ldc + gcol) * OUT_ELEM,
+                                      v.x, v.y, v.z, v.w);
                         }
                     }
                 }
@@ -854,6 +858,39 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
                 const int64_t grow_own = ts.row0 + r;
                 if (grow_own < ts.row_end && col0 < p.N)
                     p.h_s[static_cast<int64_t>(col0 / 128) * p.rows + grow_own] = tsc.s;
+                if constexpr (DEFER_STORE) {
+                    // the store warp writes the codes: stage them as the BF16 path does, in two
+                    // 32-row x 64-byte blocks, once the store warp has read the previous tile
+                    const bool freed = mbar_wait(ofree, (tile_n & 1u) ^ 1u, abort_addr, budget);
+                    if (!__all_sync(0xffffffffu, freed)) {
+                        if (lane == 0) raise_error(p.err, abort_addr, DEV_TIMEOUT_EPILOGUE);
+                        break;
+                    }
+#pragma unroll
+                    for (int g = 0; g < 2; g++) {
+#pragma unroll
+                        for (int jc = 0; jc < 4; jc++) {
+                            uint32_t w4[4];
+#pragma unroll
+                            for (int e = 0; e < 4; e++) {
+                                const int q = g * 32 + jc * 8 + 2 * e;
+                                const uint32_t lo =
+                                    cvt_e4m3x2(tile_scaled(f32x2_lo(acc[q]), tsc),
+                                               tile_scaled(f32x2_hi(acc[q]), tsc));
+                                const uint32_t hi =
+                                    cvt_e4m3x2(tile_scaled(f32x2_lo(acc[q + 1]), tsc),
+                                               tile_scaled(f32x2_hi(acc[q + 1]), tsc));
+                                w4[e] = tsc.zero ? 0u : (lo | (hi << 16));
+                            }
+                            st_shared_v4(d_buf + g * STG_WARP_BYTES + lane * 64 +
+                                             ((jc ^ ((lane >> 1) & 3)) * 16),
+                                         make_uint4(w4[0], w4[1], w4[2], w4[3]));
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(ostaged);
+                    continue;
+                }
                 const uint32_t stg = base + L::STG_OFF + (warp - EPI_WARP0) * STG_WARP_BYTES;
                 const int64_t wrow0 = ts.row0 + quad * 32;
 #pragma unroll
@@ -1101,6 +1138,9 @@ cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b,
     case GemmKind::GROUPED_SWIGLU:
         return launch_one<true, false, false, false, true>(map_a, map_b, map_c, args, max_ctas, stream);
     case GemmKind::DENSE_QUANT:
+        if (store_warp)
+            return launch_one<false, false, DP, false, false, true, true>(map_a, map_b, map_c, args,
+                                                                          max_ctas, stream);
         return launch_one<false, false, DP, false, false, true>(map_a, map_b, map_c, args, max_ctas,
                                                                 stream);
     case GemmKind::ROW_SCALED:

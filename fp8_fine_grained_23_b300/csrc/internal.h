@@ -103,8 +103,9 @@ cudaError_t launch_gemm_small(const CUtensorMap& map_w, const CUtensorMap& map_a
 enum class GemmKind { DENSE, GROUPED, ROW_SCALED, GROUPED_SWIGLU, DENSE_QUANT };
 // map_c: the output C as BF16 / FP32 with 64-byte boxes of 32 rows (make_out_map); read by the
 // kinds whose output is BF16 or FP32 (not GROUPED_SWIGLU or DENSE_QUANT, which take any map).
-// store_warp: DENSE with BF16 output only, the variant whose output tiles are written by a
-// store warp while the epilogue goes on (for K loops of 32+ blocks and 4+ tiles per pair).
+// store_warp: DENSE with BF16 output or DENSE_QUANT only, the variant whose output tiles are
+// written by a store warp while the epilogue goes on (for K loops of 32+ blocks and 4+ tiles per
+// pair).
 cudaError_t launch_gemm(const CUtensorMap& map_a, const CUtensorMap& map_b,
                         const CUtensorMap& map_c, const GemmArgs& args, GemmKind kind,
                         bool out_f32, int max_ctas, cudaStream_t stream,
