@@ -19,7 +19,7 @@
 //   warp 2     scale loader: per K block, cp.async copies of the tile's 128 activation scales
 //              and its two weight-block scales into an 8-slot shared-memory ring (sfull/sempty
 //              mbarriers), so the epilogue reads its scale from shared memory;
-//   warp 3     store warp of the DEFER variant (dense BF16 output, long K loops): writes each
+//   warp 3     store warp of the DEFER variant (dense BF16 or E4M3-code output, long K loops): writes each
 //              output tile the epilogue staged in shared memory to C while the epilogue works
 //              on the next tile; idle otherwise (warp 0 also builds the group table of the
 //              grouped variant, whose tiles follow that table built from device offsets);
@@ -54,8 +54,9 @@
 //        warp of its lane quarter and stores E4M3 codes with 1x128 scales;
 //   QO   (dense) the output re-quantized to E4M3 in 1x128 tiles: a thread's 128 columns are one
 //        tile, so amax, scale and codes are thread-local;
-//   DEFER (dense, BF16 output) output tiles written by the store warp (chosen by the host for K
-//        loops of 32+ blocks and 4+ tiles per pair; otherwise TMA bulk stores).
+//   DEFER (dense, BF16 output or QO) output tiles written by the store warp (chosen by the host
+//        for K loops of 32+ blocks and 4+ tiles per pair; otherwise TMA bulk stores for BF16, plain
+//        stores for QO).
 // (Few rows of A, M <= 64, go to the swap-AB kernel in gemm_small.cu instead.)
 //
 // Registers: the launch gives 168 per thread (65536 / 384, rounded to 8). Warpgroup 0 drops to
@@ -271,7 +272,7 @@ __device__ __forceinline__ void st_v4(void* p, uint32_t a, uint32_t b, uint32_t 
 }
 
 // QO: the output re-quantized to E4M3 in 1x128 tiles (codes to p.c, scales to p.h_s).
-// DEFER: output tiles written by the store warp (dense BF16 output only).
+// DEFER: output tiles written by the store warp (dense BF16 output or QO).
 template <bool GROUPED, bool OUT_F32, bool PAIR, bool RS, bool SW, bool QO = false,
           bool DEFER = false>
 __global__ void __launch_bounds__(THREADS, 1)
@@ -288,7 +289,7 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     // output and the row-scaled one. The plain dense kernel with FP32 output keeps 32-column
     // TMEM chunks and plain stores (with the bulk path it spilled and ran 23% slower).
     constexpr bool BULK_STORE = !GROUPED && !SW && !QO && (RS || !OUT_F32);
-    // DEFER (dense BF16 output, chosen by the host for long K loops and several tiles per pair):
+    // DEFER (dense BF16 output or QO, chosen by the host for long K loops and several tiles per pair):
     // the epilogue stages a finished tile whole in shared memory and goes on to the next tile at
     // once; the store warp writes the staged tile to C meanwhile. (One warp needs ~2 us for a
     // tile: with short K loops it fell behind, and a pair's last tile waited for it.)
