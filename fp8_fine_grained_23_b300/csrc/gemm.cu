@@ -19,10 +19,10 @@
 //   warp 2     scale loader: per K block, cp.async copies of the tile's 128 activation scales
 //              and its two weight-block scales into an 8-slot shared-memory ring (sfull/sempty
 //              mbarriers), so the epilogue reads its scale from shared memory;
-//   warp 3     store warp of the DEFER variant (dense BF16 or E4M3-code output, long K loops): writes each
-//              output tile the epilogue staged in shared memory to C while the epilogue works
-//              on the next tile; idle otherwise (warp 0 also builds the group table of the
-//              grouped variant, whose tiles follow that table built from device offsets);
+//   warp 3     store warp of the DEFER variant (dense BF16 or E4M3-code output, long K
+//              loops): writes each output tile the epilogue staged in shared memory to C while
+//              the epilogue works on the next tile; idle otherwise (warp 0 also builds the group
+//              table of the grouped variant, whose tiles follow that table of device offsets);
 //   warps 4-11 epilogue: warp w reads TMEM lanes 32*(w%4).. (its rows) and the 128 columns
 //              128*((w-4)/4).. (one weight block). Per K block it loads the partial in 16- or
 //              32-column pieces (the next piece in flight while the current one is promoted)
@@ -289,7 +289,8 @@ fp8_blockscaled_gemm_kernel(const __grid_constant__ CUtensorMap map_a,
     // output and the row-scaled one. The plain dense kernel with FP32 output keeps 32-column
     // TMEM chunks and plain stores (with the bulk path it spilled and ran 23% slower).
     constexpr bool BULK_STORE = !GROUPED && !SW && !QO && (RS || !OUT_F32);
-    // DEFER (dense BF16 output or QO, chosen by the host for long K loops and several tiles per pair):
+    // DEFER (dense BF16 output or QO, chosen by the host for long K loops and several tiles per
+    // pair):
     // the epilogue stages a finished tile whole in shared memory and goes on to the next tile at
     // once; the store warp writes the staged tile to C meanwhile. (One warp needs ~2 us for a
     // tile: with short K loops it fell behind, and a pair's last tile waited for it.)
