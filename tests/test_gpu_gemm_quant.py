@@ -35,7 +35,9 @@ def test_requantized_output_small(F, M, N, K):
 
 
 def test_requantized_output_full_size_sampled(F):
-    """The dense workload 4096x18432x7168: 48 whole rows (all 144 output tiles each)."""
+    """The dense workload 4096x18432x7168 (the launch the host gives the store-warp variant): 48
+    whole rows (all 144 output tiles each); the same launch into a wider code buffer writes the
+    same codes and nothing past N."""
     shape = W.DENSE
     a, w = W.gemm_inputs(shape, "cuda")
     aq, a_s = F.fp8_quant_act_1x128(a)
@@ -52,3 +54,8 @@ def test_requantized_output_full_size_sampled(F):
     sel = torch.from_numpy(rows).cuda()
     check_requant_tiles(cq[sel].cpu().numpy(), cs[:, sel].cpu().numpy().T, c64,
                         gemm_tolerance(c64, cabs, "f32"), "dense 4096x18432x7168 sampled rows")
+    buf = torch.full((shape.M, shape.N + 64), 0xA5, dtype=torch.uint8, device="cuda")
+    cq2, cs2 = F.fp8_blockscaled_gemm_quant(aq, a_s, wq, w_s, c_q=buf[:, :shape.N])
+    assert F.fp8bs_last_error() == F.FP8BS_OK
+    assert torch.equal(cq2, cq) and torch.equal(cs2, cs)
+    assert bool(torch.all(buf[:, shape.N:] == 0xA5))
